@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for decode-phase hybrid sparse attention.
+
+This module only draws random numbers and lays them out in the paged-KV
+format; it holds none of the attention / selection arithmetic.  Both the CUDA
+path (through the C-ABI binding) and the fp64 oracle consume what it returns.
+
+Recipe (the value distributions are a reading of the workloads the pages
+describe; no public dataset is reproduced):
+
+* Q, K, V entries are N(0, 1).  The softmax scale is 1/sqrt(D).  (The
+  "scaled 1/sqrt(128)" in the workload text is read as the softmax scale.)
+* GQA realism: inside a KV-head group, q_h = sqrt(.5) z_g + sqrt(.5) z_h with
+  z_g shared by the group.  The group direction is
+  g_hat = normalise(mean_h q_h) * sqrt(D).
+* Attention sink: key 0 of every (sequence, KV head) gets + c_sink * g_hat.
+  The sink phenomenon is the one the Fluxion page measures (Fig. 3c, Fig. 4).
+* Heavy blocks: a set of candidate blocks (block size of that KV head) whose
+  every key gets + c_heavy * g_hat.
+* Recency bias (optional): key t in the last R tokens gets + ramp(t) * g_hat,
+  ramp rising linearly from 0 to 1 (HGCA: recent entries dominate attention).
+* The page table is a seeded random permutation of physical pages, so the
+  gather through it is a real scatter over the pool.
+
+Draw order (fixed, so a seed reproduces a case): group noise z_g, head noise
+z_h, K pool, V pool, page permutation, heavy-block picks.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import torch
+
+HEAD_DIM = 128
+PAGE_SIZE = 16
+
+
+@dataclass
+class Workload:
+    """One decode-attention workload: shapes, selection settings, planted structure."""
+
+    name: str
+    B: int
+    Hq: int
+    Hk: int
+    L: int                          # tokens in the cache, current token included
+    block_sizes: List[int]          # per KV head, each in {8, 16, 32, 64}
+    budget_bp: List[int]            # per KV head, budget in basis points of candidate blocks
+    S: int = 4                      # attention-sink tokens
+    W: int = 1024                   # recent window
+    D: int = HEAD_DIM
+    P: int = PAGE_SIZE
+    mode: str = "minmax"            # block summary kind: "minmax" or "mean"
+    c_sink: float = 2.0
+    c_heavy: float = 1.5
+    heavy_count: Optional[int] = None    # fixed number of heavy blocks per (b, kv head)
+    heavy_frac: float = 0.01             # else this fraction of candidate blocks
+    recency: int = 0                     # length of the recency ramp (0 = none)
+    extra_tokens: int = 0                # page-table room for appended tokens
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hk
+
+    @property
+    def max_pages_per_seq(self) -> int:
+        return (self.L + self.extra_tokens + self.P - 1) // self.P
+
+
+def _draw_block_settings(Hk: int, seed: int):
+    g = torch.Generator().manual_seed(10_000 + seed)
+    sizes = [8, 16, 32, 64]
+    bs = [sizes[int(torch.randint(0, 4, (1,), generator=g))] for _ in range(Hk)]
+    bp = [int(torch.randint(200, 2001, (1,), generator=g)) for _ in range(Hk)]
+    return bs, bp
+
+
+def workload(name: str) -> Workload:
+    """The named workloads.  Shapes follow the Llama-3.1-8B / Qwen2.5-7B
+    attention layers and the 32K / 5 % budget / batch-8 setting of the Fluxion
+    time breakdown (Fig. 2)."""
+    if name == "tiny_4k":
+        return Workload(name, B=1, Hq=8, Hk=2, L=4096, block_sizes=[16, 16],
+                        budget_bp=[1000, 1000], S=4, W=256, c_heavy=2.0, heavy_count=3)
+    if name == "llama_32k":
+        return Workload(name, B=8, Hq=32, Hk=8, L=32768, block_sizes=[16] * 8,
+                        budget_bp=[500] * 8, S=4, W=1024, c_heavy=1.5,
+                        heavy_frac=0.01, recency=2048)
+    if name == "qwen_64k":
+        bs, bp = _draw_block_settings(4, 2)
+        return Workload(name, B=16, Hq=28, Hk=4, L=65536, block_sizes=bs,
+                        budget_bp=bp, S=4, W=1024, c_heavy=1.5, heavy_frac=0.01,
+                        recency=2048)
+    raise KeyError(name)
+
+
+# --------------------------------------------------------------------------
+# partition helpers (pure integer bookkeeping, shared by the harness)
+# --------------------------------------------------------------------------
+
+def candidate_range(L: int, S: int, W: int, Bs: int):
+    """Block index range [j0, j1) of blocks that intersect the middle region
+    M = [min(S, L), max(L - W, min(S, L)))."""
+    s_end = min(S, L)
+    w_beg = max(L - W, s_end)
+    if w_beg <= s_end:
+        return 0, 0
+    return s_end // Bs, (w_beg + Bs - 1) // Bs
+
+
+def budget_k(bp: int, ncand: int) -> int:
+    """k = ceil(bp / 10000 * ncand) in exact integer arithmetic."""
+    return min(ncand, (bp * ncand + 9999) // 10000)
+
+
+def k_per_qhead(wl: Workload, L: Optional[int] = None) -> List[int]:
+    L = wl.L if L is None else L
+    ks = []
+    for h in range(wl.Hq):
+        kvh = h // wl.G
+        j0, j1 = candidate_range(L, wl.S, wl.W, wl.block_sizes[kvh])
+        ks.append(budget_k(wl.budget_bp[kvh], j1 - j0))
+    return ks
+
+
+# --------------------------------------------------------------------------
+# the generator
+# --------------------------------------------------------------------------
+
+@dataclass
+class DecodeCase:
+    wl: Workload
+    q: torch.Tensor            # bf16 [B, Hq, D]
+    k_pool: torch.Tensor       # bf16 [num_pages, Hk, P, D]
+    v_pool: torch.Tensor       # bf16 [num_pages, Hk, P, D]
+    page_table: torch.Tensor   # int32 [B, max_pages_per_seq]
+    seq_lens: torch.Tensor     # int32 [B]
+    g_hat: torch.Tensor        # float32 [B, Hk, D]
+    heavy: List[List[List[int]]] = field(default_factory=list)  # [b][kvh] -> block ids
+
+
+def make_decode_case(wl: Workload, seed: int, device="cpu") -> DecodeCase:
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    B, Hq, Hk, G, D, P = wl.B, wl.Hq, wl.Hk, wl.G, wl.D, wl.P
+    f32 = torch.float32
+
+    z_g = torch.randn(B, Hk, 1, D, generator=g, device=dev, dtype=f32)
+    z_h = torch.randn(B, Hk, G, D, generator=g, device=dev, dtype=f32)
+    q = math.sqrt(0.5) * z_g + math.sqrt(0.5) * z_h              # [B, Hk, G, D]
+    mean_q = q.mean(dim=2)                                        # [B, Hk, D]
+    g_hat = mean_q / mean_q.norm(dim=-1, keepdim=True) * math.sqrt(D)
+    q_bf = q.reshape(B, Hq, D).to(torch.bfloat16).contiguous()
+
+    mpp = wl.max_pages_per_seq
+    num_pages = B * mpp
+    k_pool = torch.randn(num_pages, Hk, P, D, generator=g, device=dev, dtype=f32)
+    v_pool = torch.randn(num_pages, Hk, P, D, generator=g, device=dev, dtype=f32)
+    perm = torch.randperm(num_pages, generator=g, device=dev)
+    page_table = perm.reshape(B, mpp).to(torch.int32)
+
+    L = wl.L
+    npg = (L + P - 1) // P
+    heavy_all = []
+    for b in range(B):
+        coef = torch.zeros(Hk, npg * P, device=dev, dtype=f32)
+        heavy_b = []
+        for kvh in range(Hk):
+            Bs = wl.block_sizes[kvh]
+            j0, j1 = candidate_range(L, wl.S, wl.W, Bs)
+            ncand = j1 - j0
+            if wl.heavy_count is not None:
+                nh = min(wl.heavy_count, ncand)
+            else:
+                nh = min(ncand, max(1, int(round(wl.heavy_frac * ncand))))
+            picks = (torch.randperm(ncand, generator=g, device=dev)[:nh] + j0).tolist() if ncand else []
+            picks = sorted(picks)
+            heavy_b.append(picks)
+            for j in picks:
+                coef[kvh, j * Bs:(j + 1) * Bs] += wl.c_heavy
+            if L > 0:
+                coef[kvh, 0] += wl.c_sink
+            if wl.recency > 0:
+                r0 = max(0, L - wl.recency)
+                n = L - r0
+                coef[kvh, r0:L] += torch.linspace(0.0, 1.0, n, device=dev, dtype=f32)
+        heavy_all.append(heavy_b)
+        coef[:, L:] = 0.0
+        rows = page_table[b, :npg].long()
+        blk = k_pool[rows]                                          # [npg, Hk, P, D]
+        add = coef.reshape(Hk, npg, P).permute(1, 0, 2).unsqueeze(-1) * g_hat[b].reshape(1, Hk, 1, D)
+        k_pool[rows] = blk + add
+
+    seq_lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    return DecodeCase(wl=wl, q=q_bf, k_pool=k_pool.to(torch.bfloat16),
+                      v_pool=v_pool.to(torch.bfloat16), page_table=page_table,
+                      seq_lens=seq_lens, g_hat=g_hat, heavy=heavy_all)
