@@ -1,0 +1,208 @@
+/*
+ * sa.h -- C ABI of libsa: decode-phase hybrid sparse attention over a paged
+ * bf16 KV cache, hand-written CUDA for sm_103a (GB300).
+ *
+ * What the library computes, and where the pages define it:
+ *   - Dense attention over the attention sinks and the recent window, sparse
+ *     attention over selected older entries, merged exactly by the
+ *     log-sum-exp identity  O = (e^lse_I O_I + e^lse_J O_J)/(e^lse_I + e^lse_J),
+ *     lse_S = log sum_{j in S} e^{s_j}.
+ *     ("HGCA: Hybrid GPU-CPU Attention for Long Context LLM Inference", review
+ *     section "What carries the argument"; minor comment on Sec. 3.3.)
+ *   - Per-head top-k selection of fixed-size KV blocks under a head-specific
+ *     block size and budget.  ("An Efficient Hybrid Sparse Attention with
+ *     CPU-GPU Parallelism for Long-Context Inference" (Fluxion), core claim,
+ *     Fig. 2, Fig. 5.)
+ *   - KV kept in fixed-size pages reached through a page table.  ("Unifying
+ *     Sparse Attention with Hierarchical Memory for Scalable Long-Context LLM
+ *     Serving", abstract and Fig. 6.)
+ *   - Vertical / slash score tables with decay 0.95 and positional expansion
+ *     by offsets {-1,0,1,2}.  ("Learn from the Past: Fast Sparse Indexing for
+ *     Large Language Model Decoding", "What carries the argument", Eq. (9),
+ *     Eq. (10).)
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *     never allocates or frees them.  `stream` is a cudaStream_t passed as
+ *     void* (NULL = legacy default stream).  Calls are asynchronous on it.
+ *   - Dtypes are fixed: Q, K, V and block summaries bf16 (passed as void*);
+ *     scores, outputs, lse, logits and score tables fp32; indices, page tables,
+ *     lengths and counts int32.  All tensors are dense, row-major, no padding.
+ *   - Notation: B sequences, Hq query heads, Hk KV heads, G = Hq / Hk query
+ *     heads per KV head (query head h uses KV head h / G), D = 128, P = page
+ *     size (16), L = seq_lens[b] tokens in the cache INCLUDING the current
+ *     token (L must not exceed max_pages_per_seq * P), S sinks, W window,
+ *     Bs = block size of a KV head.
+ *     Dense set I = [0, min(S,L)) U [max(L-W, min(S,L)), L); middle region M
+ *     = the tokens between.  Candidate blocks are the blocks that meet M:
+ *     j in [min(S,L)/Bs, ceil(max(L-W, min(S,L))/Bs)).  A selected block
+ *     contributes only its tokens inside M, so I and the sparse set are
+ *     disjoint.
+ *   - KV pool layout: [num_pages][Hk][P][D] bf16 (one page of one KV head is a
+ *     contiguous P x D slab).  Page table: [B][max_pages_per_seq] int32,
+ *     logical page -> physical page.  Token t of sequence b is row t % P of
+ *     physical page page_table[b][t / P].
+ *   - Return value: SA_OK or an SA_ERR_* code.  Errors a host can see (bad
+ *     arguments, unsupported shapes, capacity) return BEFORE any launch.
+ *     Errors only the device can see (a page-table entry outside
+ *     [0, num_pages), a bounded wait that ran out) set a status word in the
+ *     workspace; the offending work is skipped, nothing traps.  Read it with
+ *     sa_get_status().
+ *   - Scratch comes from a caller-allocated workspace of sa_workspace_size()
+ *     bytes, zeroed once with sa_workspace_init().  Calls that share one
+ *     workspace must be ordered on one stream.
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SA_OK 0
+#define SA_ERR_INVALID_ARG 1
+#define SA_ERR_UNSUPPORTED 2
+#define SA_ERR_CUDA 3
+#define SA_ERR_CAPACITY 4
+#define SA_ERR_BAD_PAGE 5
+#define SA_ERR_TIMEOUT 6
+
+/* block summary kinds */
+#define SA_SUMMARY_MINMAX 0 /* [..][2][D]: row 0 = per-dim min, row 1 = per-dim max */
+#define SA_SUMMARY_MEAN 1   /* [..][D]: bf16(RNE(fp32 ascending sum / n)) */
+
+/* granularity of a selection list handed to sa_sparse_decode */
+#define SA_SEL_BLOCK 0 /* entries are block indices of the head's KV head */
+#define SA_SEL_TOKEN 1 /* entries are token positions */
+
+/* sa_block_summarize: block_begin value meaning "only the block holding the
+ * newest token L-1" (the incremental per-step refresh) */
+#define SA_BLOCKS_TAIL (-1)
+
+/* limits of this build */
+#define SA_HEAD_DIM 128
+#define SA_PAGE_SIZE 16
+#define SA_MAX_GROUP 8   /* G <= 8 */
+#define SA_MAX_HK 64
+#define SA_MAX_HQ 256
+
+/* Shapes and selection settings of one attention layer.  Host memory. */
+typedef struct sa_problem {
+  int32_t B;                   /* sequences */
+  int32_t Hq;                  /* query heads */
+  int32_t Hk;                  /* KV heads; Hq % Hk == 0, Hq / Hk <= 8 */
+  int32_t D;                   /* head dim; must be 128 */
+  int32_t page_size;           /* must be 16 */
+  int32_t max_pages_per_seq;   /* columns of the page table */
+  int32_t num_pages;           /* physical pages in each pool */
+  int32_t sink;                /* S >= 0 */
+  int32_t window;              /* W >= max block size */
+  int32_t summary_mode;        /* SA_SUMMARY_MINMAX or SA_SUMMARY_MEAN */
+  const int32_t* block_size_per_kvh; /* host [Hk], each in {8,16,32,64} */
+  const int32_t* k_per_qhead;        /* host [Hq], blocks kept per head, 0 <= k <= kcap */
+  int32_t kcap;                /* capacity of a selection list (entries per head) */
+  float scale;                 /* softmax scale, normally 1/sqrt(D) */
+} sa_problem;
+
+/* Block slots per (sequence, KV head) in the summary and score tensors:
+ * ceil(max_pages_per_seq * page_size / min block size).  Block j of KV head
+ * kvh of sequence b lives at slot [b][kvh][j].  0 if prob is invalid. */
+int32_t sa_block_slots(const sa_problem* prob);
+
+/* Workspace bytes for calls on this problem (0 if prob is invalid). */
+size_t sa_workspace_size(const sa_problem* prob);
+
+/* Zero a workspace (async on stream).  Needed once before first use and after
+ * any call that reported SA_ERR_TIMEOUT. */
+int sa_workspace_init(void* ws, size_t bytes, void* stream);
+
+/* Synchronise `stream`, read the device status word of `ws` into *status
+ * (SA_OK if no device-side error since the last read) and clear it. */
+int sa_get_status(void* ws, void* stream, int* status);
+
+/* Human-readable message for a status code (static storage). */
+const char* sa_status_string(int status);
+
+/* Step a1 -- block summaries.
+ * For every (b, kvh) and block j in [block_begin, block_end) clipped to
+ * [0, ceil(L/Bs)), summarise tokens [j Bs, min((j+1) Bs, L)) of K:
+ * MINMAX writes summaries[b][kvh][j][0][:] = min, [1][:] = max (exact);
+ * MEAN writes summaries[b][kvh][j][:] = bf16(RNE(fp32 sum in ascending token
+ * order / n)).  block_end = -1 means through the last block; block_begin =
+ * SA_BLOCKS_TAIL means only the block holding token L-1 (per-step refresh).
+ * Layout: [B][Hk][sa_block_slots][2][D] (MINMAX) or [B][Hk][slots][D] (MEAN),
+ * bf16.  The pages do not define the summary; this is the min/max bounding
+ * box or the mean key (Fluxion core claim: block-level selection).
+ * Device errors: a bad page id sets SA_ERR_BAD_PAGE, the block is written 0. */
+int sa_block_summarize(const sa_problem* prob, const void* k_pool,
+                       const int32_t* page_table, const int32_t* seq_lens,
+                       int32_t block_begin, int32_t block_end, void* summaries,
+                       void* ws, void* stream);
+
+/* Step a2 -- block scores.  For every (b, query head h) and candidate block j:
+ * MINMAX  s = sum_d q_d * (q_d >= 0 ? kmax_d : kmin_d)
+ * MEAN    s = sum_d q_d * kmean_d
+ * in fp32 in the canonical order: the 128 dims form 8 lanes of 16
+ * consecutive dims, each lane sums its exact products in ascending dim order
+ * (one rounding per step), the 8 lane sums are combined by a butterfly with
+ * partner offsets 4, 2, 1, and +0.0 is added.  Unscaled.
+ * scores: [B][Hq][sa_block_slots] fp32; only candidate slots are written. */
+int sa_score_blocks(const sa_problem* prob, const void* q,
+                    const void* summaries, const int32_t* seq_lens,
+                    float* scores, void* ws, void* stream);
+
+/* Steps a2 + a3 -- fused score and per-head top-k.  For every (b, h): keep
+ * k_h = min(k_per_qhead[h], ncand) candidate blocks, ranked by score
+ * descending then block index ascending, written ascending to
+ * sel_idx[b][h][0..k_h) with sel_cnt[b][h] = k_h.  If k_h == ncand the head
+ * keeps every candidate without scoring (a 100 % budget is dense attention).
+ * sel_idx: [B][Hq][kcap] int32; sel_cnt: [B][Hq] int32.
+ * scores_or_null: if not NULL, the scores are also written as in
+ * sa_score_blocks.  Requires k_per_qhead[h] <= kcap (else SA_ERR_CAPACITY). */
+int sa_select_topk(const sa_problem* prob, const void* q,
+                   const void* summaries, const int32_t* seq_lens,
+                   int32_t* sel_idx, int32_t* sel_cnt, float* scores_or_null,
+                   void* ws, void* stream);
+
+/* Steps a4 + a5 + a6 -- paged gather split-K decode attention with the exact
+ * log-sum-exp merge.  For every (b, h): attend q[b][h] over I plus the
+ * head's selected set J_h = (entries of sel_idx[b][h][0..sel_cnt)) inside M,
+ * with z_t = scale * q.k_t:
+ *   out[b][h][:] = sum_t softmax(z)_t v_t  (fp32), lse[b][h] = log sum e^{z_t}.
+ * Entries outside M or beyond L are ignored; duplicates count once.  The KV
+ * rows of the union over a KV head's G query heads are read once.  Work is
+ * split into chunks whose partial (max, sum, O) are combined with the
+ * identity above by the last chunk to finish.  An empty attended set (L = 0)
+ * gives out = 0, lse = -inf.
+ * sel_granularity: SA_SEL_BLOCK (entries are blocks of the KV head's Bs) or
+ *   SA_SEL_TOKEN (entries are positions).
+ * logits_or_null: if not NULL, [B][Hq][max_pages_per_seq*P] fp32 receives the
+ *   natural-log-domain logit z_t at every attended position t (other positions
+ *   untouched).  Used to feed the score-table update.
+ * out: [B][Hq][D] fp32; lse: [B][Hq] fp32 (natural log). */
+int sa_sparse_decode(const sa_problem* prob, const void* q,
+                     const void* k_pool, const void* v_pool,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     const int32_t* sel_idx, const int32_t* sel_cnt,
+                     int32_t sel_granularity, float* out, float* lse,
+                     float* logits_or_null, void* ws, void* stream);
+
+/* Step a6 standalone -- merge two partial attentions over disjoint sets:
+ * m = max(lse_a, lse_b), w_x = e^{lse_x - m},
+ * o = (w_a o_a + w_b o_b) / (w_a + w_b), lse = m + log(w_a + w_b);
+ * a side with lse = -inf contributes nothing; both -inf gives o = 0,
+ * lse = -inf.  o_*: [n_rows][D] fp32; lse_*: [n_rows] fp32.  Output may alias
+ * an input.  (HGCA review, "What carries the argument" and Sec. 3.3.) */
+int sa_lse_merge(int32_t n_rows, int32_t D, const float* o_a,
+                 const float* lse_a, const float* o_b, const float* lse_b,
+                 float* o, float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

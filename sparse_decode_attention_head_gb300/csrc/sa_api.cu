@@ -1,0 +1,280 @@
+// The C ABI of libsa (declared in include/sa.h): argument validation,
+// workspace layout, TMA descriptors, and the launches.  Everything a host can
+// check is checked here, before any launch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "sa_common.cuh"
+
+namespace sa {
+int launch_summarize(const Params& p, const void* k_pool, const int* page_table, const int* seq_lens,
+                     int block_begin, int block_end, void* summ, int* status, cudaStream_t stream);
+int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
+                 int always, cudaStream_t stream);
+int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
+                cudaStream_t stream);
+size_t topk_smem_bytes(const Params& p);
+int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
+                       void* tiles, int* ntiles, cudaStream_t stream);
+int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
+                  float* partials, int* counters, float* out, float* lse, float* logits, int* status,
+                  const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
+size_t decode_smem_bytes(int U);
+int chunk_cap_of(const Params& p);
+size_t tiles_bytes(const Params& p);
+int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
+                     const float* lse_b, float* o, float* lse, cudaStream_t stream);
+}  // namespace sa
+
+using sa::Params;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Validate a problem and fill the launch parameters.
+int make_params(const sa_problem* pr, Params* p) {
+  if (pr == nullptr) return SA_ERR_INVALID_ARG;
+  if (pr->B < 1 || pr->Hq < 1 || pr->Hk < 1) return SA_ERR_INVALID_ARG;
+  if (pr->Hq % pr->Hk != 0) return SA_ERR_INVALID_ARG;
+  if (pr->D != SA_HEAD_DIM) return SA_ERR_INVALID_ARG;
+  if (pr->Hq / pr->Hk > SA_MAX_GROUP || pr->Hk > SA_MAX_HK || pr->Hq > SA_MAX_HQ) return SA_ERR_UNSUPPORTED;
+  if (pr->page_size != SA_PAGE_SIZE) return SA_ERR_UNSUPPORTED;
+  if (pr->max_pages_per_seq < 1 || pr->num_pages < 1 || pr->sink < 0) return SA_ERR_INVALID_ARG;
+  if (pr->summary_mode != SA_SUMMARY_MINMAX && pr->summary_mode != SA_SUMMARY_MEAN) return SA_ERR_INVALID_ARG;
+  if (pr->block_size_per_kvh == nullptr || pr->k_per_qhead == nullptr) return SA_ERR_INVALID_ARG;
+  if (pr->kcap < 1) return SA_ERR_INVALID_ARG;
+  if (!(pr->scale > 0.f) || !std::isfinite(pr->scale)) return SA_ERR_INVALID_ARG;
+  if ((long long)pr->max_pages_per_seq * SA_PAGE_SIZE >= (1LL << 30)) return SA_ERR_UNSUPPORTED;
+  if ((long long)pr->num_pages * pr->Hk * SA_PAGE_SIZE >= (1LL << 31)) return SA_ERR_UNSUPPORTED;
+  int max_bs = 0, min_bs = 1 << 30;
+  for (int i = 0; i < pr->Hk; ++i) {
+    const int bs = pr->block_size_per_kvh[i];
+    if (bs != 8 && bs != 16 && bs != 32 && bs != 64) return SA_ERR_INVALID_ARG;
+    if (!(SA_PAGE_SIZE % bs == 0 || bs % SA_PAGE_SIZE == 0)) return SA_ERR_INVALID_ARG;
+    max_bs = std::max(max_bs, bs);
+    min_bs = std::min(min_bs, bs);
+  }
+  if (pr->window < max_bs) return SA_ERR_INVALID_ARG;   // every candidate block is then complete
+  for (int i = 0; i < pr->Hq; ++i) {
+    if (pr->k_per_qhead[i] < 0) return SA_ERR_INVALID_ARG;
+    if (pr->k_per_qhead[i] > pr->kcap) return SA_ERR_CAPACITY;
+  }
+  std::memset(p, 0, sizeof(*p));
+  p->B = pr->B;
+  p->Hq = pr->Hq;
+  p->Hk = pr->Hk;
+  p->G = pr->Hq / pr->Hk;
+  p->mpp = pr->max_pages_per_seq;
+  p->num_pages = pr->num_pages;
+  p->S = pr->sink;
+  p->W = pr->window;
+  p->mode = pr->summary_mode;
+  p->kcap = pr->kcap;
+  p->scale = pr->scale;
+  p->slots = (int)(((long long)pr->max_pages_per_seq * SA_PAGE_SIZE + min_bs - 1) / min_bs);
+  for (int i = 0; i < pr->Hk; ++i) p->bs[i] = pr->block_size_per_kvh[i];
+  for (int i = 0; i < pr->Hq; ++i) p->k[i] = pr->k_per_qhead[i];
+  return SA_OK;
+}
+
+struct Layout {
+  size_t header, scores, tiles, ntiles, counters, partials, total;
+};
+
+Layout layout_of(const Params& p) {
+  Layout l;
+  size_t off = 0;
+  l.header = off;
+  off = align_up(off + sizeof(sa::WsHeader));
+  l.scores = off;
+  off = align_up(off + (size_t)p.B * p.Hq * p.slots * sizeof(float));
+  l.tiles = off;
+  off = align_up(off + sa::tiles_bytes(p));
+  l.ntiles = off;
+  off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.counters = off;
+  off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.partials = off;
+  off = align_up(off + (size_t)p.B * p.Hk * sa::chunk_cap_of(p) * p.G * (SA_HEAD_DIM + 2) * sizeof(float));
+  l.total = off;
+  return l;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Pool [num_pages][Hk][P][D] bf16 viewed as rows of D; boxes of 16 rows x 64.
+int make_kv_map(CUtensorMap* m, const void* pool, const Params& p) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return SA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)SA_HEAD_DIM, (cuuint64_t)p.num_pages * p.Hk * SA_PAGE_SIZE};
+  cuuint64_t strides[1] = {(cuuint64_t)SA_HEAD_DIM * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int32_t sa_block_slots(const sa_problem* prob) {
+  Params p;
+  if (make_params(prob, &p) != SA_OK) return 0;
+  return p.slots;
+}
+
+size_t sa_workspace_size(const sa_problem* prob) {
+  Params p;
+  if (make_params(prob, &p) != SA_OK) return 0;
+  return layout_of(p).total;
+}
+
+int sa_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (ws == nullptr || bytes < sizeof(sa::WsHeader)) return SA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, bytes, as_stream(stream)) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+int sa_get_status(void* ws, void* stream, int* status) {
+  if (ws == nullptr || status == nullptr) return SA_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SA_ERR_CUDA;
+  *status = v;
+  return SA_OK;
+}
+
+const char* sa_status_string(int status) {
+  switch (status) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported shape or setting";
+    case SA_ERR_CUDA: return "CUDA runtime error";
+    case SA_ERR_CAPACITY: return "capacity exceeded";
+    case SA_ERR_BAD_PAGE: return "page-table entry outside the pool";
+    case SA_ERR_TIMEOUT: return "bounded device wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int sa_block_summarize(const sa_problem* prob, const void* k_pool, const int32_t* page_table,
+                       const int32_t* seq_lens, int32_t block_begin, int32_t block_end, void* summaries,
+                       void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!k_pool || !page_table || !seq_lens || !summaries || !ws) return SA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (block_begin < 0 && block_begin != SA_BLOCKS_TAIL) return SA_ERR_INVALID_ARG;
+  if (block_end < -1) return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  return sa::launch_summarize(p, k_pool, page_table, seq_lens, block_begin, block_end, summaries,
+                              at<int>(ws, l.header), as_stream(stream));
+}
+
+int sa_score_blocks(const sa_problem* prob, const void* q, const void* summaries, const int32_t* seq_lens,
+                    float* scores, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !summaries || !seq_lens || !scores || !ws) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  return sa::launch_score(p, q, summaries, seq_lens, scores, 1, as_stream(stream));
+}
+
+int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries, const int32_t* seq_lens,
+                   int32_t* sel_idx, int32_t* sel_cnt, float* scores_or_null, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !summaries || !seq_lens || !sel_idx || !sel_cnt || !ws) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (sa::topk_smem_bytes(p) > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  const Layout l = layout_of(p);
+  float* scores = scores_or_null ? scores_or_null : at<float>(ws, l.scores);
+  cudaStream_t s = as_stream(stream);
+  rc = sa::launch_score(p, q, summaries, seq_lens, scores, scores_or_null != nullptr, s);
+  if (rc != SA_OK) return rc;
+  return sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s);
+}
+
+int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel_idx,
+                     const int32_t* sel_cnt, int32_t sel_granularity, float* out, float* lse,
+                     float* logits_or_null, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !sel_idx || !sel_cnt || !out || !lse || !ws)
+    return SA_ERR_INVALID_ARG;
+  if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return SA_ERR_INVALID_ARG;
+  if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SA_ERR_CUDA;
+  CUtensorMap tmK, tmV;
+  if ((rc = make_kv_map(&tmK, k_pool, p)) != SA_OK) return rc;
+  if ((rc = make_kv_map(&tmV, v_pool, p)) != SA_OK) return rc;
+  const Layout l = layout_of(p);
+  cudaStream_t s = as_stream(stream);
+  rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
+                              at<int>(ws, l.ntiles), s);
+  if (rc != SA_OK) return rc;
+  return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
+                           at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
+                           at<int>(ws, l.header), tmK, tmV, nsm, s);
+}
+
+int sa_lse_merge(int32_t n_rows, int32_t D, const float* o_a, const float* lse_a, const float* o_b,
+                 const float* lse_b, float* o, float* lse, void* stream) {
+  if (n_rows < 0 || D < 1) return SA_ERR_INVALID_ARG;
+  if (n_rows == 0) return SA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse) return SA_ERR_INVALID_ARG;
+  return sa::launch_lse_merge(n_rows, D, o_a, lse_a, o_b, lse_b, o, lse, as_stream(stream));
+}
+
+}  // extern "C"
