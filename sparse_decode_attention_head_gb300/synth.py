@@ -58,6 +58,7 @@ class Workload:
     heavy_frac: float = 0.01             # else this fraction of candidate blocks
     recency: int = 0                     # length of the recency ramp (0 = none)
     extra_tokens: int = 0                # page-table room for appended tokens
+    lens: Optional[List[int]] = None     # per-sequence lengths (ragged batch); default all L
 
     @property
     def G(self) -> int:
@@ -160,10 +161,14 @@ def make_decode_case(wl: Workload, seed: int, device="cpu") -> DecodeCase:
     perm = torch.randperm(num_pages, generator=g, device=dev)
     page_table = perm.reshape(B, mpp).to(torch.int32)
 
-    L = wl.L
-    npg = (L + P - 1) // P
+    lens = list(wl.lens) if wl.lens is not None else [wl.L] * B
     heavy_all = []
     for b in range(B):
+        L = lens[b]
+        npg = (L + P - 1) // P
+        if npg == 0:
+            heavy_all.append([[] for _ in range(Hk)])
+            continue
         coef = torch.zeros(Hk, npg * P, device=dev, dtype=f32)
         heavy_b = []
         for kvh in range(Hk):
@@ -192,7 +197,7 @@ def make_decode_case(wl: Workload, seed: int, device="cpu") -> DecodeCase:
         add = coef.reshape(Hk, npg, P).permute(1, 0, 2).unsqueeze(-1) * g_hat[b].reshape(1, Hk, 1, D)
         k_pool[rows] = blk + add
 
-    seq_lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
     return DecodeCase(wl=wl, q=q_bf, k_pool=k_pool.to(torch.bfloat16),
                       v_pool=v_pool.to(torch.bfloat16), page_table=page_table,
                       seq_lens=seq_lens, g_hat=g_hat, heavy=heavy_all)

@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/sa.h declares, and rejects bad arguments on the host before any
+launch (these calls never reach the GPU)."""
+import ctypes
+import os
+
+import pytest
+
+from sparse_decode_attention_head_gb300 import build_lib, sa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(sa.LIB_PATH):
+        build_lib.build()
+    return sa.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = sa.header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _prob(**kw):
+    base = dict(B=2, Hq=8, Hk=2, max_pages_per_seq=64, num_pages=128, sink=4, window=64,
+                block_sizes=[16, 16], k_per_head=[3] * 8, kcap=8)
+    base.update(kw)
+    return sa.Problem(**base)
+
+
+def test_sizes_of_a_valid_problem(lib):
+    p = _prob(block_sizes=[8, 32])
+    assert p.block_slots() == 64 * 16 // 8
+    assert p.workspace_size() > 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=7), sa.SA_ERR_INVALID_ARG),                  # Hq % Hk != 0
+    (dict(D=64), sa.SA_ERR_INVALID_ARG),                  # D != 128
+    (dict(block_sizes=[16, 12]), sa.SA_ERR_INVALID_ARG),  # Bs not in {8,16,32,64}
+    (dict(window=8), sa.SA_ERR_INVALID_ARG),              # W < max Bs
+    (dict(k_per_head=[-1] + [3] * 7), sa.SA_ERR_INVALID_ARG),
+    (dict(k_per_head=[9] + [3] * 7), sa.SA_ERR_CAPACITY),  # k > kcap
+    (dict(page_size=32), sa.SA_ERR_UNSUPPORTED),
+    (dict(Hq=32, Hk=2, k_per_head=[1] * 32), sa.SA_ERR_UNSUPPORTED),  # G = 16 > 8
+    (dict(kcap=0), sa.SA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), sa.SA_ERR_INVALID_ARG),
+])
+def test_host_validation_before_launch(lib, kw, code):
+    p = _prob(**kw)
+    assert p.workspace_size() == 0
+    vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    rc = lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, vp, None)
+    assert rc == code
+    rc = lib.sa_select_topk(p.ref, vp, vp, vp, vp, vp, None, vp, None)
+    assert rc == code
+    rc = lib.sa_block_summarize(p.ref, vp, vp, vp, 0, -1, vp, vp, None)
+    assert rc == code
+
+
+def test_null_pointers_rejected(lib):
+    p = _prob()
+    vp = ctypes.c_void_p(16)
+    assert lib.sa_sparse_decode(p.ref, None, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 5, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_score_blocks(p.ref, vp, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_block_summarize(p.ref, vp, vp, vp, -5, -1, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_lse_merge(-1, 128, vp, vp, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_lse_merge(0, 128, None, None, None, None, None, None, None) == sa.SA_OK
+    assert lib.sa_workspace_size(None) == 0
+
+
+def test_status_strings(lib):
+    for c in range(7):
+        assert sa.status_string(c) not in ("", "unknown status")
+    assert sa.status_string(99) == "unknown status"
