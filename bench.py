@@ -1,0 +1,421 @@
+"""Benchmark: one decode step of hybrid sparse attention on the Llama-3.1-8B
+shaped 32K layer (B=8, 32 query / 8 KV heads, D=128, page = block = 16,
+5 % budget, 4 sinks, 1024-token window), bf16 paged KV.
+
+A step is the whole hot path for one layer:
+  tail-block summary refresh -> fused block score + per-head top-k ->
+  paged sparse decode (dense sinks + window, sparse selected blocks, exact
+  log-sum-exp merge of the split-K partials).
+Eight independent layer copies (8.6 GB of KV) rotate from step to step, so
+nothing a step reads is still in the 129 MB L2 when it is read again.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_decode_attention_head_gb300 import sa, synth  # noqa: E402
+
+WORKLOAD = "llama_32k"
+N_LAYERS = 8   # default; --layers overrides
+METRIC = "decode attn queries/s & achieved HBM GB/s (% of 8 TB/s), Llama-3-8B shape 32K"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = os.path.join(ROOT, "profiles", "sparse_decode_llama_32k.md")
+
+
+# --------------------------------------------------------------------------- helpers
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "sa_common.cuh"):
+        with open(os.path.join(ROOT, "sparse_decode_attention_head_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def algorithmic_bytes(wl, prob, seq_lens, sel_idx, sel_cnt):
+    """Per-step algorithmic HBM bytes, split by call (byte accounting of the
+    hot-path scope: summaries of candidate blocks, KV rows of I U (union of the
+    group's selected blocks) once per group, q, O + lse, page-table entries)."""
+    P, D, G = wl.P, wl.D, wl.G
+    si, sc = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
+    dec = sel = summ = 0
+    for b in range(wl.B):
+        L = int(seq_lens[b])
+        s_end = min(wl.S, L)
+        w_beg = max(L - wl.W, s_end)
+        for kvh in range(wl.Hk):
+            Bs = wl.block_sizes[kvh]
+            j0, j1 = synth.candidate_range(L, wl.S, wl.W, Bs)
+            toks = set(range(0, s_end)) | set(range(w_beg, L))
+            for g in range(G):
+                h = kvh * G + g
+                for j in si[b, h, :sc[b, h]]:
+                    toks.update(range(max(j * Bs, s_end), min((j + 1) * Bs, w_beg)))
+            pages = {t // P for t in toks}
+            dec += len(toks) * 2 * D * 2 + G * D * 2 + G * (D * 4 + 4) + len(pages) * 4
+            summ_row = 2 * D * 2 if prob.mode == sa.SUMMARY_MINMAX else D * 2
+            sel += (j1 - j0) * summ_row + G * D * 2 + G * 4 * (1 + int(np.mean(sc[b, kvh * G:(kvh + 1) * G])))
+            summ += Bs * D * 2 + summ_row + ((Bs + P - 1) // P) * 4
+    return {"decode": dec, "select": sel, "summary": summ, "total": dec + sel + summ}
+
+
+def run_ours(args):
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    sa.lib()
+
+    wl = synth.workload(WORKLOAD)
+    ks = synth.k_per_qhead(wl)
+    kcap = max(ks)
+    prob = sa.Problem(B=wl.B, Hq=wl.Hq, Hk=wl.Hk, max_pages_per_seq=wl.max_pages_per_seq,
+                      num_pages=wl.B * wl.max_pages_per_seq, sink=wl.S, window=wl.W,
+                      block_sizes=wl.block_sizes, k_per_head=ks, kcap=kcap, mode=sa.SUMMARY_MINMAX)
+    ws = sa.Workspace(prob, device=dev)
+
+    global N_LAYERS
+    N_LAYERS = args.layers
+    layers = []
+    for l in range(N_LAYERS):
+        c = synth.make_decode_case(wl, 1000 * rank + 100 + l, device=dev)
+        summ = torch.empty(prob.summary_shape(), dtype=torch.bfloat16, device=dev)
+        sa.block_summarize(prob, c.k_pool, c.page_table, c.seq_lens, summ, ws)   # one-time full build
+        layers.append(dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens, summ=summ,
+                           sel_idx=torch.empty(wl.B, wl.Hq, kcap, dtype=torch.int32, device=dev),
+                           sel_cnt=torch.empty(wl.B, wl.Hq, dtype=torch.int32, device=dev)))
+        del c
+    torch.cuda.synchronize()
+    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32, device=dev)
+    lse = torch.empty(wl.B, wl.Hq, dtype=torch.float32, device=dev)
+
+    def sub_select(L):
+        sa.block_summarize(prob, L["k"], L["pt"], L["sl"], L["summ"], ws, block_begin=sa.BLOCKS_TAIL)
+        sa.select_topk(prob, L["q"], L["summ"], L["sl"], L["sel_idx"], L["sel_cnt"], ws)
+
+    def sub_decode(L):
+        sa.sparse_decode(prob, L["q"], L["k"], L["v"], L["pt"], L["sl"], L["sel_idx"], L["sel_cnt"], out, lse, ws)
+
+    # eager warm-up (sets kernel attributes, selection for the byte count)
+    for L in layers:
+        sub_select(L)
+        sub_decode(L)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    nbytes = [algorithmic_bytes(wl, prob, L["sl"].cpu().numpy(), L["sel_idx"], L["sel_cnt"]) for L in layers]
+
+    # one CUDA graph per (layer, sub-step): the timed loop only replays
+    stream = torch.cuda.Stream(device=dev)
+    g_sel, g_dec = [], []
+    with torch.cuda.stream(stream):
+        for L in layers:
+            g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream, capture_error_mode="relaxed"):
+                sub_select(L)
+            with torch.cuda.graph(g2, stream=stream, capture_error_mode="relaxed"):
+                sub_decode(L)
+            g_sel.append(g1)
+            g_dec.append(g2)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            g_sel[i % N_LAYERS].replay()
+            g_dec[i % N_LAYERS].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            l = (W + i) % N_LAYERS
+            ev[i][0].record(stream)
+            g_sel[l].replay()
+            ev[i][1].record(stream)
+            g_dec[l].replay()
+            ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    sel_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    queries = wl.B * wl.Hq
+    value = world * queries * K / (total_ms / 1e3)
+
+    layer_of = [(W + i) % N_LAYERS for i in range(K)]
+    dec_bytes = float(np.mean([nbytes[l]["decode"] for l in layer_of]))
+    step_bytes = float(np.mean([nbytes[l]["total"] for l in layer_of]))
+    dec_avg_ms = float(np.mean(dec_ms))
+    peak, peak_src = measured_hbm_peak()
+    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+
+    # end to end through the public binding: pinned host q in, O + lse out
+    e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
+
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V with planted sink, heavy blocks and recency ramp)",
+        "config": {"workload": "llama3.1-8b layer, decode, B8 x 32q/8kv heads x D128, ctx 32768, "
+                               "page=block=16, budget 5% (k=100 blocks), sinks 4, window 1024, minmax summaries",
+                   "global_batch": wl.B, "seq_len": wl.L, "parallelism": f"replicas x{world}",
+                   "l2": f"{N_LAYERS} rotating independent layer copies ({N_LAYERS * 1.07:.1f} GB KV), inputs > L2"},
+        "roofline": {"bound": "hbm", "kernel": "sa_sparse_decode (tile build + paged decode + split-K merge)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": int(dec_bytes), "avg_launch_ms": round(dec_avg_ms, 5)},
+        "step_roofline": {"achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+                          "frac": round(step_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
+                          "algorithmic_bytes_per_step": int(step_bytes),
+                          "select_avg_ms": round(float(np.mean(sel_ms)), 5)},
+        "e2e": e2e,
+        "gpu_launches": 5 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(layers[0], wl, ks, prob.scale, budget_s=args.cpu_seconds)
+        cb.pop("queries")
+        res["cpu_baseline"] = cb
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(args, prob, layers, ws, out, lse, dev):
+    wl_B, Hq, D = prob.B, prob.Hq, prob.D
+    q_host = [L["q"].cpu().pin_memory() for L in layers]
+    o_host = torch.empty(wl_B, Hq, D, dtype=torch.float32).pin_memory()
+    l_host = torch.empty(wl_B, Hq, dtype=torch.float32).pin_memory()
+    K, W = args.steps, args.warmup
+
+    def step(i):
+        L = layers[i % N_LAYERS]
+        L["q"].copy_(q_host[i % N_LAYERS], non_blocking=True)
+        sa.block_summarize(prob, L["k"], L["pt"], L["sl"], L["summ"], ws, block_begin=sa.BLOCKS_TAIL)
+        sa.select_topk(prob, L["q"], L["summ"], L["sl"], L["sel_idx"], L["sel_cnt"], ws)
+        sa.sparse_decode(prob, L["q"], L["k"], L["v"], L["pt"], L["sl"], L["sel_idx"], L["sel_cnt"], out, lse, ws)
+        o_host.copy_(out, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        step(W + i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(wl_B * Hq * K / (ms / 1e3), 1), "unit": "queries/s",
+            "h2d_bytes_per_step": wl_B * Hq * D * 2, "d2h_bytes_per_step": wl_B * Hq * (D + 1) * 4,
+            "ms_per_step": round(ms / K, 5), "path": "python binding -> C-ABI, eager launches"}
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def cpu_baseline(L, wl, ks, scale, budget_s=15.0, units=None):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the same
+    workload: selection + decode for whole (sequence, KV head) units."""
+    from oracle import sparse_attention_oracle as orc
+    from tests import harness as H
+
+    nc = H.NpCase(q=orc.to_np(L["q"]), k_pool=orc.to_np(L["k"]), v_pool=orc.to_np(L["v"]),
+                  page_table=orc.to_np(L["pt"]), seq_lens=orc.to_np(L["sl"]))
+    all_units = [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
+    done = 0
+    t0 = time.perf_counter()
+    for u in (units or all_units):
+        sel = H.oracle_select(nc, wl, ks, "minmax", units=[u])
+        H.oracle_decode(nc, wl, {k: v[0] for k, v in sel.items()}, sa.SEL_BLOCK, scale, units=[u])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    q = done * wl.G
+    return {"value": round(q / dt, 2), "unit": "queries/s", "cores": 1, "kind": "oracle", "queries": q,
+            "sample": f"{done} of {len(all_units)} (sequence, KV head) units = {q} queries of one layer "
+                      f"step (summaries + canonical scores + top-k + fp64 attention + merge), {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return
+    wl = synth.workload(WORKLOAD)
+    ks = synth.k_per_qhead(wl)
+    c = synth.make_decode_case(wl, 100)
+    L = dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    units = [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
+    for i in range(args.warmup):
+        cpu_baseline(L, wl, ks, 1 / math.sqrt(wl.D), budget_s=0.0, units=units[i % len(units):][:1])
+    t0 = time.perf_counter()
+    nq = 0
+    for i in range(args.steps):
+        r = cpu_baseline(L, wl, ks, 1 / math.sqrt(wl.D), budget_s=per_step, units=units)
+        nq += r["queries"]
+    dt = time.perf_counter() - t0
+    v = round(nq / dt, 2)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "llama3.1-8b layer, decode, B8 x 32q/8kv, ctx 32768, 5% budget",
+                                        "global_batch": wl.B, "seq_len": wl.L, "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{nq} queries over {args.steps} steps, each a bounded sample of (sequence, KV "
+                                   f"head) units of one layer step"},
+        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="independent layer copies rotated per step (1.07 GB of KV each)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
