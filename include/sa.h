@@ -191,6 +191,32 @@ int sa_sparse_decode(const sa_problem* prob, const void* q,
                      int32_t sel_granularity, float* out, float* lse,
                      float* logits_or_null, void* ws, void* stream);
 
+/* Sparse decode without a workspace.  The pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory and so
+ * cannot hand sa_sparse_decode a workspace -- for example code running inside
+ * a host framework that owns every device allocation through its own pool,
+ * or a latency-critical path where cudaMalloc's implicit synchronisation is
+ * not allowed.  Same inputs, outputs and results as sa_sparse_decode; the
+ * scratch lives in a fixed 64 MiB array of device memory inside the library
+ * (held by every GPU that loads the library until the process exits).
+ * The call allocates nothing.  A problem whose scratch does not fit returns
+ * SA_ERR_CAPACITY before any launch.
+ * status_or_null: optional device int32 that receives the first device-side
+ *   error of this call (SA_OK otherwise); it is zeroed at the start of the
+ *   call.  When NULL, device-side errors are recorded only inside the library.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents (the counters and status it needs zeroed are cleared at the
+ * start of each call): calls that overlap on the GPU race with each other. */
+int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* page_table, const int32_t* seq_lens,
+                             const int32_t* sel_idx, const int32_t* sel_cnt,
+                             int32_t sel_granularity, float* out, float* lse,
+                             float* logits_or_null, int32_t* status_or_null,
+                             void* stream);
+
 /* Step a6 standalone -- merge two partial attentions over disjoint sets:
  * m = max(lse_a, lse_b), w_x = e^{lse_x - m},
  * o = (w_a o_a + w_b o_b) / (w_a + w_b), lse = m + log(w_a + w_b);

@@ -1,0 +1,132 @@
+// sa_sparse_decode_noalloc: the sparse decode step for callers that cannot
+// allocate device memory.
+//
+// sa_sparse_decode needs a caller-allocated workspace for its scratch (the
+// per-KV-head tile lists, the split-K partials and their arrival counters).
+// Some callers cannot provide one: code that runs inside a host framework
+// which owns every device allocation through its own pool and forbids any
+// other cudaMalloc, or a latency-critical path where cudaMalloc's implicit
+// device synchronisation is not allowed.  This entry point takes the same
+// inputs and outputs but keeps its scratch in one fixed-size array in device
+// global memory that belongs to this library (kNoAllocScratchBytes per GPU,
+// held by every GPU that loads the library until the process exits).
+//
+// Host code cannot use the array's name as a device address, so the first
+// call on each device looks the address up with cudaGetSymbolAddress (with
+// that device current) and caches it.  Every call shares the array and it
+// keeps the last call's contents: the arrival counters and the status word
+// are cleared at the start of each call, and two calls that overlap on the
+// GPU (different streams, or different host threads) race on it.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "sa_common.cuh"
+
+namespace sa {
+int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
+                       void* tiles, int* ntiles, cudaStream_t stream);
+int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
+                  float* partials, int* counters, float* out, float* lse, float* logits, int* status,
+                  const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
+size_t decode_smem_bytes(int U);
+int chunk_cap_of(const Params& p);
+size_t tiles_bytes(const Params& p);
+}  // namespace sa
+
+namespace sa_host {
+int make_params(const sa_problem* pr, sa::Params* p);
+int make_kv_map(CUtensorMap* m, const void* pool, const sa::Params& p);
+int num_sms_current();
+}  // namespace sa_host
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;   // 64 MiB per device
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct NoAllocLayout {
+  size_t status, counters, ntiles, tiles, partials, total;
+};
+
+NoAllocLayout layout_of(const sa::Params& p) {
+  NoAllocLayout l;
+  size_t off = 0;
+  l.status = off;
+  off = up256(off + sizeof(int));
+  l.counters = off;
+  off = up256(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.ntiles = off;
+  off = up256(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.tiles = off;
+  off = up256(off + sa::tiles_bytes(p));
+  l.partials = off;
+  off = up256(off + (size_t)p.B * p.Hk * sa::chunk_cap_of(p) * p.G * (SA_HEAD_DIM + 2) * sizeof(float));
+  l.total = off;
+  return l;
+}
+
+// Device address of the scratch array on the current device (set-up on first use).
+int scratch_on_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return SA_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return SA_OK;
+}
+
+inline bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* page_table, const int32_t* seq_lens,
+                                        const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_granularity,
+                                        float* out, float* lse, float* logits_or_null, int32_t* status_or_null,
+                                        void* stream) {
+  sa::Params p;
+  int rc = sa_host::make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !sel_idx || !sel_cnt || !out || !lse)
+    return SA_ERR_INVALID_ARG;
+  if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return SA_ERR_INVALID_ARG;
+  if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const NoAllocLayout l = layout_of(p);
+  if (l.total > kNoAllocScratchBytes) return SA_ERR_CAPACITY;   // problem too large for the fixed scratch
+  void* base = nullptr;
+  if ((rc = scratch_on_current_device(&base)) != SA_OK) return rc;
+  const int nsm = sa_host::num_sms_current();
+  if (nsm <= 0) return SA_ERR_CUDA;
+  CUtensorMap tmK, tmV;
+  if ((rc = sa_host::make_kv_map(&tmK, k_pool, p)) != SA_OK) return rc;
+  if ((rc = sa_host::make_kv_map(&tmV, v_pool, p)) != SA_OK) return rc;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* b = static_cast<char*>(base);
+  int* status = status_or_null ? status_or_null : reinterpret_cast<int*>(b + l.status);
+  int* counters = reinterpret_cast<int*>(b + l.counters);
+  // what must start at zero: the status word and the split-K arrival counters
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
+  if (cudaMemsetAsync(counters, 0, (size_t)p.B * p.Hk * sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
+  rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
+                              reinterpret_cast<int*>(b + l.ntiles), s);
+  if (rc != SA_OK) return rc;
+  return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
+                           reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,
+                           tmK, tmV, nsm, s);
+}

@@ -33,7 +33,8 @@ int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, co
 
 using sa::Params;
 
-namespace {
+// Host-side helpers (also used by noalloc.cu).
+namespace sa_host {
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -155,7 +156,9 @@ int num_sms_current() {
 
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-}  // namespace
+}  // namespace sa_host
+
+using namespace sa_host;
 
 extern "C" {
 

@@ -75,6 +75,7 @@ def lib():
             "sa_select_topk": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_lse_merge": (ctypes.c_int, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
