@@ -16,13 +16,18 @@
 // tile is one 16-token page with a G-bit head mask per token, so the rows a
 // GQA group shares are read once (SPIN abstract / Fig. 6: paged KV substrate).
 //
-// Kernel 2 (decode, persistent): work items are (KV head unit, chunk of up to
-// kTPC tiles).  Lanes of warp 0 look up the page table and issue 2-D TMA
-// loads (SWIZZLE_128B, 2 boxes of 16 x 64 bf16 per 4 KB page slab of K and of
-// V) completing on one mbarrier per tile.  Each warp then takes whole tiles:
-// S = K Q^T and O^T += V^T P on mma.sync m16n8k16 (tokens x heads, heads
-// padded to 8), with P split into a bf16 high part and a bf16 residual so the
-// product keeps ~16 mantissa bits.
+// Kernel 2 (decode, persistent, stream-K): the tile lists of all units are
+// concatenated and every CTA takes an equal contiguous slice, so the load is
+// balanced whatever the union sizes are.  A producer warp keeps a ring of
+// kSlots page slots full: it looks up the page table and issues 2-D TMA loads
+// (SWIZZLE_128B, two 16 x 64 bf16 boxes per 4 KB slab of K and of V) that
+// complete on the slot's "full" mbarrier.  Consumer warps take the slice's
+// tiles round-robin: S = K Q^T and O^T += V^T P on mma.sync m16n8k16 (tokens x
+// heads, heads padded to 8), with P split into a bf16 high part and a bf16
+// residual so the product keeps ~16 mantissa bits; they release the slot on
+// its "empty" mbarrier.  At the end of each unit segment the consumer warps
+// merge their states; a unit split over several CTAs leaves one partial per
+// CTA, and the last CTA to finish merges them in CTA order (deterministic).
 #include <cuda.h>
 
 #include <algorithm>
@@ -38,9 +43,11 @@ struct __align__(16) Tile {
 };
 
 constexpr int kBuildThreads = 512;
-constexpr int kDecWarps = 4;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kTPC = 8;                      // tiles per chunk
+constexpr int kConsWarps = 4;                      // consumer warps
+constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
+constexpr int kSlots = 8;                          // ring slots; a multiple of kConsWarps (see below)
+constexpr int kMaxCtas = 1024;                     // grid cap (partial slots are sized for it)
+constexpr int kPart = kD + 2;                      // floats per head in a partial: O[kD], max, sum
 constexpr int kSlab = kP * kD * 2;           // 4096 bytes: one page of one KV head
 constexpr int kTileBytes = 2 * kSlab;        // K + V
 constexpr int kBoxBytes = 16 * 64 * 2;       // one TMA box: 16 rows x 64 bf16
@@ -63,7 +70,7 @@ __device__ __forceinline__ void item_range(int gran, int x, int Bs, int Lc, int 
 __global__ void __launch_bounds__(kBuildThreads)
 build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ sel_idx,
                    const int* __restrict__ sel_cnt, int gran, Tile* __restrict__ tiles,
-                   int* __restrict__ ntiles) {
+                   int* __restrict__ ntiles, float* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ int flag[];  // [mpp]: page flag, then tile index
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -172,6 +179,10 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
     }
   }
   if (tid == 0) ntiles[u] = total;
+  if (total == 0) {   // nothing attended (L = 0): O = 0, lse = -inf; the decode kernel skips the unit
+    for (int i = tid; i < G * kD; i += blockDim.x) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
+    if (tid < G) lse[(size_t)b * p.Hq + kvh * G + tid] = -INFINITY;
+  }
 }
 
 // ------------------------------------------------------------------ decode
@@ -181,13 +192,17 @@ struct DecodeArgs {
   const int* page_table;
   const Tile* tiles;
   const int* ntiles;
-  float* partials;   // [U][chunk_cap][G][kD + 2]
+  float* partials;   // [kMaxCtas][2][G][kPart]
   int* counters;     // [U]
   float* out;
   float* lse;
   float* logits;     // may be null
   int* status;
-  int chunk_cap;
+};
+
+struct __align__(16) SlotInfo {
+  int unit, lp, phys, pad;
+  uint32_t mask[4];
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -196,83 +211,137 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)((chunk >> 3) * kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ int nchunks_of(int nt) { return nt > 0 ? (nt + kTPC - 1) / kTPC : 1; }
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsWarps * 32) : "memory");
+}
 
-__global__ void __launch_bounds__(kDecThreads)
+// CTA whose slice [c T / n, (c+1) T / n) holds global tile x.
+__device__ __forceinline__ int cta_of(long long x, long long T, int n) {
+  return (int)(((x + 1) * n + T - 1) / T) - 1;
+}
+
+__device__ __forceinline__ long long slice_lo(int c, long long T, int n) { return (long long)c * T / n; }
+
+// Unit u with prefix[u] <= x < prefix[u + 1] (prefix non-decreasing, x < prefix[U]).
+__device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
+  int lo = 0, hi = U;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-byte aligned base for the swizzled TMA boxes
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_tiles = smem;                                          // kTPC * kTileBytes
-  uint8_t* s_p = s_tiles + kTPC * kTileBytes;                       // kDecWarps * 512 bytes
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_p + kDecWarps * 512);   // kTPC
-  int* s_phys = reinterpret_cast<int*>(s_bar + kTPC);                // kTPC
-  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_phys + kTPC);     // kTPC * 4
-  int* s_lp = reinterpret_cast<int*>(s_mask + 4 * kTPC);             // kTPC
-  int* s_misc = s_lp + kTPC;                                         // [0] last flag, [1] abort
-  int* s_prefix = s_misc + 4;                                        // [U + 1]
+  uint8_t* s_tiles = smem;                                                   // kSlots * kTileBytes
+  uint8_t* s_p = s_tiles + kSlots * kTileBytes;                              // kConsWarps * 512
+  float* s_w = reinterpret_cast<float*>(s_p + kConsWarps * 512);             // kConsWarps * 8 * kPart
+  SlotInfo* s_info = reinterpret_cast<SlotInfo*>(s_w + kConsWarps * 8 * kPart);   // kSlots
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_info + kSlots);           // kSlots
+  uint64_t* s_empty = s_full + kSlots;                                       // kSlots
+  int* s_misc = reinterpret_cast<int*>(s_empty + kSlots);                    // 32 ints
+  int* s_prefix = s_misc + 32;                                               // U + 1
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
   const int U = p.B * p.Hk;
 
   if (tid == 0) {
-    for (int i = 0; i < kTPC; ++i) mbar_init(&s_bar[i], 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 1);
+    }
     fence_mbar_init();
-    s_misc[1] = 0;
   }
-  // work prefix over units: chunks per unit
-  for (int i = tid; i < U; i += blockDim.x) s_prefix[i + 1] = nchunks_of(A.ntiles[i]);
-  __syncthreads();
-  if (tid == 0) {
-    s_prefix[0] = 0;
-    for (int i = 0; i < U; ++i) s_prefix[i + 1] += s_prefix[i];
+  // prefix over the units' tile counts (block-wide scan)
+  {
+    const int per = (U + blockDim.x - 1) / blockDim.x;
+    const int a = min(U, tid * per), e = min(U, a + per);
+    int cnt = 0;
+    for (int i = a; i < e; ++i) cnt += A.ntiles[i];
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_misc[warp] = x;
+    __syncthreads();
+    int before = x - cnt;
+    for (int w2 = 0; w2 < warp; ++w2) before += s_misc[w2];
+    for (int i = a; i < e; ++i) {
+      s_prefix[i] = before;
+      before += A.ntiles[i];
+    }
+    if (tid == blockDim.x - 1) s_prefix[U] = before;
   }
   __syncthreads();
-  const int total = s_prefix[U];
-  uint32_t phase = 0;   // bit i = parity of the next phase of barrier i
+  const long long T = s_prefix[U];
+  const int nC = gridDim.x, c = blockIdx.x;
+  const long long lo = slice_lo(c, T, nC), hi = slice_lo(c + 1, T, nC);
+  if (lo >= hi) return;
+  const int n_local = (int)(hi - lo);
+
+  // ------------------------------------------------------------ producer warp
+  if (warp == kConsWarps) {
+    for (int i0 = 0; i0 < n_local; i0 += kSlots) {
+      const int i = i0 + lane;
+      if (lane < kSlots && i < n_local) {
+        const long long t = lo + i;
+        const int u = unit_of(s_prefix, U, t);
+        const int b = u / p.Hk, kvh = u % p.Hk;
+        const Tile* tp = A.tiles + (size_t)u * p.mpp + (t - s_prefix[u]);
+        const int4 w0 = __ldg(reinterpret_cast<const int4*>(tp));
+        const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
+        const int lp = w0.x;
+        const int phys = (lp >= 0 && lp < p.mpp) ? __ldg(A.page_table + (size_t)b * p.mpp + lp) : -1;
+        const bool ok = phys >= 0 && phys < p.num_pages;
+        if (!ok) set_status(A.status, SA_ERR_BAD_PAGE);
+        const int slot = i % kSlots, use = i / kSlots;
+        const bool free_slot = use == 0 || mbar_wait_bounded(&s_empty[slot], (use - 1) & 1, A.status);
+        if (free_slot) {
+        SlotInfo info;
+        info.unit = u;
+        info.lp = lp;
+        info.phys = ok ? phys : -1;
+        info.pad = 0;
+        info.mask[0] = w1.x; info.mask[1] = w1.y; info.mask[2] = w1.z; info.mask[3] = w1.w;
+        s_info[slot] = info;
+        if (ok) {
+          uint8_t* dst = s_tiles + slot * kTileBytes;
+          const int row = (phys * p.Hk + kvh) * kP;
+          mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
+          tma_load_2d(dst, &tmK, 0, row, &s_full[slot]);
+          tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_full[slot]);
+          tma_load_2d(dst + kSlab, &tmV, 0, row, &s_full[slot]);
+          tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_full[slot]);
+        } else {
+          mbar_arrive(&s_full[slot]);
+        }
+        }
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer warps
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int g4 = lane >> 2, t4 = lane & 3;
+  uint8_t* sp = s_p + warp * 512;
+  const uint32_t sp_hi = smem_u32(sp), sp_lo = sp_hi + 256;
+  const int tc = tid;   // consumer thread index == head-dim index in the merges (kConsWarps * 32 == kD)
 
-  for (int w = blockIdx.x; w < total; w += gridDim.x) {
-    // locate the unit: s_prefix[lo] <= w < s_prefix[lo + 1]
-    int lo = 0, hi = U;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= w) lo = mid; else hi = mid;
-    }
-    const int u = lo;
-    const int c = w - s_prefix[u];
-    const int nch = s_prefix[u + 1] - s_prefix[u];
+  for (int u = unit_of(s_prefix, U, lo); u < U && s_prefix[u] < hi; ++u) {
+    const long long ub = s_prefix[u], ue = s_prefix[u + 1];
+    const long long sb = max(lo, ub), se = min(hi, ue);
+    if (sb >= se) continue;
     const int b = u / p.Hk, kvh = u % p.Hk;
-    const int nt = A.ntiles[u];
-    const int t_begin = c * kTPC;
-    const int t_cnt = max(0, min(kTPC, nt - t_begin));
 
-    // ---- producer: warp 0 lanes look up pages and issue the TMA loads
-    if (warp == 0 && lane < t_cnt) {
-      const Tile* tp = A.tiles + (size_t)u * p.mpp + t_begin + lane;
-      const int4 w0 = *reinterpret_cast<const int4*>(tp);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(&tp->mask[0]);
-      const int lp = w0.x;
-      const int phys = (lp >= 0 && lp < p.mpp) ? A.page_table[(size_t)b * p.mpp + lp] : -1;
-      const bool ok = phys >= 0 && phys < p.num_pages;
-      if (!ok) set_status(A.status, SA_ERR_BAD_PAGE);
-      s_phys[lane] = ok ? phys : -1;
-      s_lp[lane] = lp;
-      s_mask[4 * lane + 0] = w1.x; s_mask[4 * lane + 1] = w1.y;
-      s_mask[4 * lane + 2] = w1.z; s_mask[4 * lane + 3] = w1.w;
-      if (ok) {
-        uint8_t* dst = s_tiles + lane * kTileBytes;
-        const int row = (phys * p.Hk + kvh) * kP;
-        mbar_arrive_expect_tx(&s_bar[lane], kTileBytes);
-        tma_load_2d(dst, &tmK, 0, row, &s_bar[lane]);
-        tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_bar[lane]);
-        tma_load_2d(dst + kSlab, &tmV, 0, row, &s_bar[lane]);
-        tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_bar[lane]);
-      }
-    }
     // Q fragments (B operand: k = dim, n = head), heads >= G are zero
     uint32_t qb[8][2];
     {
@@ -285,102 +354,105 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         qb[ks][1] = hv ? __ldg(qrow + ks * 8 + 4 + t4) : 0u;
       }
     }
-    __syncthreads();
-
-    // ---- consumers: each warp takes whole tiles
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    uint8_t* sp = s_p + warp * 512;
-    const uint32_t sp_hi = smem_u32(sp), sp_lo = sp_hi + 256;
 
-    for (int i = warp; i < t_cnt; i += kDecWarps) {
-      if (s_phys[i] < 0) continue;
-      if (!mbar_wait_bounded(&s_bar[i], (phase >> i) & 1u, A.status)) {
-        s_misc[1] = 1;
-        continue;
-      }
-      const uint32_t sK = smem_u32(s_tiles + i * kTileBytes);
-      const uint32_t sV = sK + kSlab;
-      // S = K Q^T  (rows = tokens, cols = heads)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int mi = lane >> 3, r = lane & 7;
-        const int row = (mi & 1) * 8 + r;
+    const int ib = (int)(sb - lo), ie = (int)(se - lo);
+    for (int i = ib + ((warp - ib % kConsWarps) + kConsWarps) % kConsWarps; i < ie; i += kConsWarps) {
+      // i % kConsWarps == warp, and kSlots % kConsWarps == 0, so the previous use of
+      // this slot was consumed by this same warp: a parity wait cannot alias
+      const int slot = i % kSlots, use = i / kSlots;
+      const bool ok = mbar_wait_bounded(&s_full[slot], use & 1, A.status);
+      if (!ok) mbar_wait_bounded(&s_full[slot], use & 1, A.status);   // give a late copy a chance to land
+      const SlotInfo info = s_info[slot];
+      if (ok && info.phys >= 0) {
+        const uint32_t sK = smem_u32(s_tiles + slot * kTileBytes);
+        const uint32_t sV = sK + kSlab;
+        // S = K Q^T  (rows = tokens, cols = heads), two accumulators to halve the chain
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int mi = lane >> 3, r = lane & 7;
+          const int row = (mi & 1) * 8 + r;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(sK + swz(row, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
-          mma_bf16_16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          for (int ks = 0; ks < 8; ks += 2) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(sK + swz(row, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
+            mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            ldsm_x4(sK + swz(row, (ks + 1) * 2 + (mi >> 1)), a0, a1, a2, a3);
+            mma_bf16_16816(sb2, a0, a1, a2, a3, qb[ks + 1][0], qb[ks + 1][1]);
+          }
         }
-      }
-      // masks: tokens g4 and g4 + 8, heads 2 t4 and 2 t4 + 1
-      const uint32_t mb0 = (s_mask[4 * i + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
-      const uint32_t mb1 = (s_mask[4 * i + 2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
-      const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-      const bool v00 = (mb0 >> h0) & 1u, v01 = (mb0 >> h1) & 1u;
-      const bool v10 = (mb1 >> h0) & 1u, v11 = (mb1 >> h1) & 1u;
-      const float z00 = v00 ? s[0] * scale_log2 : -INFINITY;
-      const float z01 = v01 ? s[1] * scale_log2 : -INFINITY;
-      const float z10 = v10 ? s[2] * scale_log2 : -INFINITY;
-      const float z11 = v11 ? s[3] * scale_log2 : -INFINITY;
-      float t0 = fmaxf(z00, z10), t1 = fmaxf(z01, z11);
+        const float s0 = sa[0] + sb2[0], s1 = sa[1] + sb2[1], s2 = sa[2] + sb2[2], s3 = sa[3] + sb2[3];
+        // masks: tokens g4 and g4 + 8, heads 2 t4 and 2 t4 + 1
+        const uint32_t mb0 = (info.mask[g4 >> 2] >> (8 * (g4 & 3))) & 0xffu;
+        const uint32_t mb1 = (info.mask[2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        const bool v00 = (mb0 >> h0) & 1u, v01 = (mb0 >> h1) & 1u;
+        const bool v10 = (mb1 >> h0) & 1u, v11 = (mb1 >> h1) & 1u;
+        const float z00 = v00 ? s0 * scale_log2 : -INFINITY;
+        const float z01 = v01 ? s1 * scale_log2 : -INFINITY;
+        const float z10 = v10 ? s2 * scale_log2 : -INFINITY;
+        const float z11 = v11 ? s3 * scale_log2 : -INFINITY;
+        float t0 = fmaxf(z00, z10), t1 = fmaxf(z01, z11);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-        t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
-      }
-      const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
-      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-      const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
-      const float p00 = exp2f(z00 - u0), p01 = exp2f(z01 - u1);
-      const float p10 = exp2f(z10 - u0), p11 = exp2f(z11 - u1);
-      l0 = l0 * al0 + p00 + p10;
-      l1 = l1 * al1 + p01 + p11;
-      m0 = n0;
-      m1 = n1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
-      }
-      if (A.logits != nullptr) {
-        const int base_tok = s_lp[i] * kP;
-        const size_t hs = (size_t)p.mpp * kP;
-        const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
-        if (v00) A.logits[row0 + h0 * hs + base_tok + g4] = s[0] * p.scale;
-        if (v01) A.logits[row0 + h1 * hs + base_tok + g4] = s[1] * p.scale;
-        if (v10) A.logits[row0 + h0 * hs + base_tok + g4 + 8] = s[2] * p.scale;
-        if (v11) A.logits[row0 + h1 * hs + base_tok + g4 + 8] = s[3] * p.scale;
-      }
-      // P (tokens x heads) as bf16 high part + bf16 residual
-      {
-        const __nv_bfloat162 hA = __floats2bfloat162_rn(p00, p01);
-        const __nv_bfloat162 hB = __floats2bfloat162_rn(p10, p11);
-        const float2 fA = __bfloat1622float2(hA), fB = __bfloat1622float2(hB);
-        uint32_t* ph = reinterpret_cast<uint32_t*>(sp);
-        uint32_t* pl = reinterpret_cast<uint32_t*>(sp + 256);
-        ph[g4 * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hA);
-        ph[(g4 + 8) * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hB);
-        pl[g4 * 4 + t4] = pack_bf16(p00 - fA.x, p01 - fA.y);
-        pl[(g4 + 8) * 4 + t4] = pack_bf16(p10 - fB.x, p11 - fB.y);
-      }
-      __syncwarp();
-      uint32_t bh0, bh1, bl0, bl1;
-      ldsm_x2_t(sp_hi + (lane & 15) * 16, bh0, bh1);
-      ldsm_x2_t(sp_lo + (lane & 15) * 16, bl0, bl1);
-      {
-        const int mi = lane >> 3, r = lane & 7;
-        const int tok = (mi >> 1) * 8 + r;
+        for (int off = 4; off < 32; off <<= 1) {
+          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+        }
+        const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+        const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
+        const float p00 = exp2f(z00 - u0), p01 = exp2f(z01 - u1);
+        const float p10 = exp2f(z10 - u0), p11 = exp2f(z11 - u1);
+        l0 = l0 * al0 + p00 + p10;
+        l1 = l1 * al1 + p01 + p11;
+        m0 = n0;
+        m1 = n1;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(sV + swz(tok, mt * 2 + (mi & 1)), a0, a1, a2, a3);
-          mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        }
+        if (A.logits != nullptr) {
+          const int base_tok = info.lp * kP;
+          const size_t hs = (size_t)p.mpp * kP;
+          const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
+          if (v00) A.logits[row0 + h0 * hs + base_tok + g4] = s0 * p.scale;
+          if (v01) A.logits[row0 + h1 * hs + base_tok + g4] = s1 * p.scale;
+          if (v10) A.logits[row0 + h0 * hs + base_tok + g4 + 8] = s2 * p.scale;
+          if (v11) A.logits[row0 + h1 * hs + base_tok + g4 + 8] = s3 * p.scale;
+        }
+        // P (tokens x heads) as bf16 high part + bf16 residual
+        {
+          const __nv_bfloat162 hA = __floats2bfloat162_rn(p00, p01);
+          const __nv_bfloat162 hB = __floats2bfloat162_rn(p10, p11);
+          const float2 fA = __bfloat1622float2(hA), fB = __bfloat1622float2(hB);
+          uint32_t* ph = reinterpret_cast<uint32_t*>(sp);
+          uint32_t* pl = reinterpret_cast<uint32_t*>(sp + 256);
+          ph[g4 * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hA);
+          ph[(g4 + 8) * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hB);
+          pl[g4 * 4 + t4] = pack_bf16(p00 - fA.x, p01 - fA.y);
+          pl[(g4 + 8) * 4 + t4] = pack_bf16(p10 - fB.x, p11 - fB.y);
+        }
+        __syncwarp();
+        uint32_t bh0, bh1, bl0, bl1;
+        ldsm_x2_t(sp_hi + (lane & 15) * 16, bh0, bh1);
+        ldsm_x2_t(sp_lo + (lane & 15) * 16, bl0, bl1);
+        {
+          const int mi = lane >> 3, r = lane & 7;
+          const int tok = (mi >> 1) * 8 + r;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(sV + swz(tok, mt * 2 + (mi & 1)), a0, a1, a2, a3);
+            mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+          }
         }
       }
-      __syncwarp();
+      __syncwarp();   // all lanes done reading the slot (and the P buffer)
+      if (lane == 0) mbar_arrive(&s_empty[slot]);
     }
     // row sums over the 8 lanes that share t4
 #pragma unroll
@@ -388,117 +460,109 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    // flip the phase of every barrier that completed in this chunk
-    for (int i = 0; i < t_cnt; ++i)
-      if (s_phys[i] >= 0) phase ^= 1u << i;
-    __syncthreads();   // all warps done with the tiles; reuse tile smem
-
-    // ---- merge the warps' states: wm/wl [kDecWarps][8], wo [kDecWarps][8][kD]
-    float* wm = reinterpret_cast<float*>(s_tiles);
-    float* wl = wm + kDecWarps * 8;
-    float* wo = wl + kDecWarps * 8;
-    if (g4 == 0) {
-      wm[warp * 8 + 2 * t4] = m0; wm[warp * 8 + 2 * t4 + 1] = m1;
-      wl[warp * 8 + 2 * t4] = l0; wl[warp * 8 + 2 * t4 + 1] = l1;
-    }
+    // ---- merge the consumer warps' states: s_w[warp][head][kPart]
+    {
+      float* ww = s_w + warp * 8 * kPart;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int d = mt * 16 + g4;
-      wo[(warp * 8 + 2 * t4) * kD + d] = o[mt][0];
-      wo[(warp * 8 + 2 * t4 + 1) * kD + d] = o[mt][1];
-      wo[(warp * 8 + 2 * t4) * kD + d + 8] = o[mt][2];
-      wo[(warp * 8 + 2 * t4 + 1) * kD + d + 8] = o[mt][3];
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d = mt * 16 + g4;
+        ww[(2 * t4) * kPart + d] = o[mt][0];
+        ww[(2 * t4 + 1) * kPart + d] = o[mt][1];
+        ww[(2 * t4) * kPart + d + 8] = o[mt][2];
+        ww[(2 * t4 + 1) * kPart + d + 8] = o[mt][3];
+      }
+      if (g4 == 0) {
+        ww[(2 * t4) * kPart + kD] = m0; ww[(2 * t4 + 1) * kPart + kD] = m1;
+        ww[(2 * t4) * kPart + kD + 1] = l0; ww[(2 * t4 + 1) * kPart + kD + 1] = l1;
+      }
     }
-    __syncthreads();
-    const int d = tid;   // kDecThreads == kD
-    float* part = A.partials + ((size_t)u * A.chunk_cap + c) * G * (kD + 2);
+    consumer_sync();
+    const bool whole = ub >= lo && ue <= hi;
+    const int pslot = ub <= lo ? 0 : 1;   // this CTA's first segment, or its last
+    float* part = A.partials + ((size_t)c * 2 + pslot) * G * kPart;
     for (int g = 0; g < G; ++g) {
       float M = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kDecWarps; ++ww) M = fmaxf(M, wm[ww * 8 + g]);
+      for (int ww = 0; ww < kConsWarps; ++ww) M = fmaxf(M, s_w[(ww * 8 + g) * kPart + kD]);
       float acc = 0.f, l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int ww = 0; ww < kDecWarps; ++ww) {
-          const float mw = wm[ww * 8 + g];
+        for (int ww = 0; ww < kConsWarps; ++ww) {
+          const float mw = s_w[(ww * 8 + g) * kPart + kD];
           const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-          acc += f * wo[(ww * 8 + g) * kD + d];
-          l += f * wl[ww * 8 + g];
+          acc += f * s_w[(ww * 8 + g) * kPart + tc];
+          l += f * s_w[(ww * 8 + g) * kPart + kD + 1];
         }
       }
-      if (nch == 1) {
+      if (whole) {
         const size_t row = (size_t)b * p.Hq + kvh * G + g;
-        A.out[row * kD + d] = l > 0.f ? acc / l : 0.f;
-        if (d == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        A.out[row * kD + tc] = l > 0.f ? acc / l : 0.f;
+        if (tc == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
       } else {
-        part[g * (kD + 2) + d] = acc;
-        if (d == 0) {
-          part[g * (kD + 2) + kD] = M;
-          part[g * (kD + 2) + kD + 1] = l;
+        part[g * kPart + tc] = acc;
+        if (tc == 0) {
+          part[g * kPart + kD] = M;
+          part[g * kPart + kD + 1] = l;
         }
       }
     }
-    if (nch > 1) {
+    if (!whole) {
       __threadfence();
-      __syncthreads();
-      if (tid == 0) {
+      consumer_sync();
+      const int c_first = cta_of(ub, T, nC), c_last = cta_of(ue - 1, T, nC);
+      if (tc == 0) {
         const int prev = atomicAdd(&A.counters[u], 1);
-        s_misc[0] = (prev == nch - 1);
+        s_misc[0] = (prev == c_last - c_first);
       }
-      __syncthreads();
+      consumer_sync();
       if (s_misc[0]) {
         __threadfence();
-        const float* pu = A.partials + (size_t)u * A.chunk_cap * G * (kD + 2);
         for (int g = 0; g < G; ++g) {
           float M = -INFINITY;
-          for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pu + ((size_t)cc * G + g) * (kD + 2) + kD));
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
+            M = fmaxf(M, __ldcg(A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart + kD));
+          }
           float acc = 0.f, l = 0.f;
           if (M != -INFINITY) {
-            for (int cc = 0; cc < nch; ++cc) {
-              const float* pc = pu + ((size_t)cc * G + g) * (kD + 2);
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
+              const float* pc = A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart;
               const float mc = __ldcg(pc + kD);
               const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-              acc += f * __ldcg(pc + d);
+              acc += f * __ldcg(pc + tc);
               l += f * __ldcg(pc + kD + 1);
             }
           }
           const size_t row = (size_t)b * p.Hq + kvh * G + g;
-          A.out[row * kD + d] = l > 0.f ? acc / l : 0.f;
-          if (d == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          A.out[row * kD + tc] = l > 0.f ? acc / l : 0.f;
+          if (tc == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
-        if (tid == 0) A.counters[u] = 0;
+        if (tc == 0) A.counters[u] = 0;
       }
     }
-    fence_proxy_async_smem();   // generic smem writes above precede the next chunk's TMA writes
-    __syncthreads();
-    if (s_misc[1]) break;       // a wait ran out: stop taking work
-  }
-  // a wait that ran out may leave copies in flight: give them a bounded
-  // chance to land before the CTA's shared memory is released
-  if (s_misc[1] && tid < kTPC) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-      if (mbar_try_wait(&s_bar[tid], (phase >> tid) & 1u)) break;
+    consumer_sync();   // s_w and s_misc are reused by the next segment
   }
 }
 
 size_t decode_smem_bytes(int U) {
-  return 1024 + (size_t)kTPC * kTileBytes + kDecWarps * 512 + kTPC * 8 + kTPC * 4 + kTPC * 16 + kTPC * 4 + 16 +
-         (size_t)(U + 1) * 4;
+  return 1024 + (size_t)kSlots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * 8 * kPart * 4 +
+         kSlots * sizeof(SlotInfo) + 2 * kSlots * 8 + 32 * 4 + (size_t)(U + 1) * 4;
 }
 
-int chunk_cap_of(const Params& p) { return (p.mpp + kTPC - 1) / kTPC; }
+size_t decode_partials_bytes(const Params& p) { return (size_t)kMaxCtas * 2 * p.G * kPart * sizeof(float); }
 
 size_t tiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * p.mpp * sizeof(Tile); }
 
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, cudaStream_t stream) {
+                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream) {
   const size_t smem = (size_t)p.mpp * sizeof(int);
   if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(build_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.Hk, p.B);
   build_tiles_kernel<<<grid, kBuildThreads, smem, stream>>>(p, seq_lens, sel_idx, sel_cnt, gran,
-                                                            static_cast<Tile*>(tiles), ntiles);
+                                                            static_cast<Tile*>(tiles), ntiles, out, lse);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -513,9 +577,7 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kDecThreads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int chunk_cap = chunk_cap_of(p);
-  const long long max_work = (long long)U * chunk_cap;
-  const int grid = (int)std::min<long long>(max_work, (long long)num_sms * per_sm);
+  const int grid = std::min(kMaxCtas, num_sms * per_sm);
   DecodeArgs A;
   A.q = static_cast<const __nv_bfloat16*>(q);
   A.page_table = page_table;
@@ -527,7 +589,6 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.lse = lse;
   A.logits = logits;
   A.status = status;
-  A.chunk_cap = chunk_cap;
   decode_kernel<<<grid, kDecThreads, smem, stream>>>(p, A, tmK, tmV);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }

@@ -25,12 +25,12 @@
 
 namespace sa {
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, cudaStream_t stream);
+                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
 size_t decode_smem_bytes(int U);
-int chunk_cap_of(const Params& p);
+size_t decode_partials_bytes(const Params& p);
 size_t tiles_bytes(const Params& p);
 }  // namespace sa
 
@@ -68,7 +68,7 @@ NoAllocLayout layout_of(const sa::Params& p) {
   l.tiles = off;
   off = up256(off + sa::tiles_bytes(p));
   l.partials = off;
-  off = up256(off + (size_t)p.B * p.Hk * sa::chunk_cap_of(p) * p.G * (SA_HEAD_DIM + 2) * sizeof(float));
+  off = up256(off + sa::decode_partials_bytes(p));
   l.total = off;
   return l;
 }
@@ -124,7 +124,7 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   if (cudaMemsetAsync(counters, 0, (size_t)p.B * p.Hk * sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
-                              reinterpret_cast<int*>(b + l.ntiles), s);
+                              reinterpret_cast<int*>(b + l.ntiles), out, lse, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
                            reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,

@@ -20,12 +20,12 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
                 cudaStream_t stream);
 size_t topk_smem_bytes(const Params& p);
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, cudaStream_t stream);
+                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
 size_t decode_smem_bytes(int U);
-int chunk_cap_of(const Params& p);
+size_t decode_partials_bytes(const Params& p);
 size_t tiles_bytes(const Params& p);
 int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                      const float* lse_b, float* o, float* lse, cudaStream_t stream);
@@ -103,7 +103,7 @@ Layout layout_of(const Params& p) {
   l.counters = off;
   off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
   l.partials = off;
-  off = align_up(off + (size_t)p.B * p.Hk * sa::chunk_cap_of(p) * p.G * (SA_HEAD_DIM + 2) * sizeof(float));
+  off = align_up(off + sa::decode_partials_bytes(p));
   l.total = off;
   return l;
 }
@@ -265,7 +265,7 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   const Layout l = layout_of(p);
   cudaStream_t s = as_stream(stream);
   rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
-                              at<int>(ws, l.ntiles), s);
+                              at<int>(ws, l.ntiles), out, lse, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
                            at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
