@@ -281,7 +281,10 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   }
   __syncthreads();
   const long long T = s_prefix[U];
-  const int nC = gridDim.x, c = blockIdx.x;
+  // slice over n_eff = min(grid, T) CTAs so that every slice is non-empty: the
+  // split-unit merge counts one arrival per CTA index between two slices
+  const int nC = (int)min((long long)gridDim.x, T), c = blockIdx.x;
+  if (c >= nC) return;
   const long long lo = slice_lo(c, T, nC), hi = slice_lo(c + 1, T, nC);
   if (lo >= hi) return;
   const int n_local = (int)(hi - lo);
