@@ -19,9 +19,10 @@
 // Kernel 2 (decode, persistent, stream-K): the tile lists of all units are
 // concatenated and every CTA takes an equal contiguous slice, so the load is
 // balanced whatever the union sizes are.  A producer warp keeps a ring of
-// kSlots page slots full: it looks up the page table and issues 2-D TMA loads
-// (SWIZZLE_128B, two 16 x 64 bf16 boxes per 4 KB slab of K and of V) that
-// complete on the slot's "full" mbarrier.  Consumer warps take the slice's
+// page slots full (one lane per slot, each running on its own): it reads the
+// tile descriptor (the builder already looked the page up) and issues 2-D TMA
+// loads (SWIZZLE_128B, two 16 x 64 bf16 boxes per 4 KB slab of K and of V)
+// that complete on the slot's "full" mbarrier.  Consumer warps take the slice's
 // tiles round-robin: S = K Q^T and O^T += V^T P on mma.sync m16n8k16 (tokens x
 // heads, heads padded to 8), with P split into a bf16 high part and a bf16
 // residual so the product keeps ~16 mantissa bits; they release the slot on
@@ -38,14 +39,14 @@ namespace sa {
 
 struct __align__(16) Tile {
   int lp;            // logical page
-  int pad[3];
+  int phys;          // physical page (page_table lookup), -1 if outside the pool
+  int pad[2];
   uint32_t mask[4];  // byte i = G-bit mask of heads attending token 16 lp + i
 };
 
 constexpr int kBuildThreads = 512;
 constexpr int kConsWarps = 4;                      // consumer warps
 constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
-constexpr int kSlots = 8;                          // ring slots; a multiple of kConsWarps (see below)
 constexpr int kMaxCtas = 1024;                     // grid cap (partial slots are sized for it)
 constexpr int kPart = kD + 2;                      // floats per head in a partial: O[kD], max, sum
 constexpr int kSlab = kP * kD * 2;           // 4096 bytes: one page of one KV head
@@ -68,9 +69,10 @@ __device__ __forceinline__ void item_range(int gran, int x, int Bs, int Lc, int 
 }
 
 __global__ void __launch_bounds__(kBuildThreads)
-build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ sel_idx,
-                   const int* __restrict__ sel_cnt, int gran, Tile* __restrict__ tiles,
-                   int* __restrict__ ntiles, float* __restrict__ out, float* __restrict__ lse) {
+build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
+                   const int* __restrict__ sel_idx, const int* __restrict__ sel_cnt, int gran,
+                   Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
+                   float* __restrict__ lse, int* status) {
   extern __shared__ int flag[];  // [mpp]: page flag, then tile index
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -133,7 +135,11 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
       // dense-set tokens of this page attend for every head
       Tile t;
       t.lp = i;
-      t.pad[0] = t.pad[1] = t.pad[2] = 0;
+      const int phys = __ldg(page_table + (size_t)b * p.mpp + i);
+      const bool ok = phys >= 0 && phys < p.num_pages;
+      if (!ok) set_status(status, SA_ERR_BAD_PAGE);
+      t.phys = ok ? phys : -1;
+      t.pad[0] = t.pad[1] = 0;
 #pragma unroll
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t m = 0;
@@ -234,16 +240,17 @@ __device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
 
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV) {
+              const __grid_constant__ CUtensorMap tmV, int nslots) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_tiles = smem;                                                   // kSlots * kTileBytes
-  uint8_t* s_p = s_tiles + kSlots * kTileBytes;                              // kConsWarps * 512
-  float* s_w = reinterpret_cast<float*>(s_p + kConsWarps * 512);             // kConsWarps * 8 * kPart
-  SlotInfo* s_info = reinterpret_cast<SlotInfo*>(s_w + kConsWarps * 8 * kPart);   // kSlots
-  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_info + kSlots);           // kSlots
-  uint64_t* s_empty = s_full + kSlots;                                       // kSlots
-  int* s_misc = reinterpret_cast<int*>(s_empty + kSlots);                    // 32 ints
+  // nslots page slots (a multiple of kConsWarps), then small state
+  uint8_t* s_tiles = smem;                                                   // nslots * kTileBytes
+  uint8_t* s_p = s_tiles + (size_t)nslots * kTileBytes;                      // kConsWarps * 512
+  float* s_w = reinterpret_cast<float*>(s_p + kConsWarps * 512);             // kConsWarps * G * kPart
+  SlotInfo* s_info = reinterpret_cast<SlotInfo*>(s_w + kConsWarps * p.G * kPart);   // nslots
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_info + nslots);           // nslots
+  uint64_t* s_empty = s_full + nslots;                                       // nslots
+  int* s_misc = reinterpret_cast<int*>(s_empty + nslots);                    // 32 ints
   int* s_prefix = s_misc + 32;                                               // U + 1
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -251,7 +258,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   const int U = p.B * p.Hk;
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < nslots; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 1);
     }
@@ -290,33 +297,30 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   const int n_local = (int)(hi - lo);
 
   // ------------------------------------------------------------ producer warp
+  // Lane j owns slot j and the tiles j, j + nslots, ... of the slice, so every
+  // slot's uses are issued in order by one thread and the lanes run freely.
   if (warp == kConsWarps) {
-    for (int i0 = 0; i0 < n_local; i0 += kSlots) {
-      const int i = i0 + lane;
-      if (lane < kSlots && i < n_local) {
+    if (lane < nslots) {
+      const int slot = lane;
+      int u = unit_of(s_prefix, U, lo + lane < hi ? lo + lane : lo);
+      for (int i = lane, use = 0; i < n_local; i += nslots, ++use) {
         const long long t = lo + i;
-        const int u = unit_of(s_prefix, U, t);
-        const int b = u / p.Hk, kvh = u % p.Hk;
+        while (t >= s_prefix[u + 1]) ++u;
         const Tile* tp = A.tiles + (size_t)u * p.mpp + (t - s_prefix[u]);
-        const int4 w0 = __ldg(reinterpret_cast<const int4*>(tp));
+        const int4 w0 = __ldg(reinterpret_cast<const int4*>(tp));       // issued before the wait below
         const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
-        const int lp = w0.x;
-        const int phys = (lp >= 0 && lp < p.mpp) ? __ldg(A.page_table + (size_t)b * p.mpp + lp) : -1;
-        const bool ok = phys >= 0 && phys < p.num_pages;
-        if (!ok) set_status(A.status, SA_ERR_BAD_PAGE);
-        const int slot = i % kSlots, use = i / kSlots;
-        const bool free_slot = use == 0 || mbar_wait_bounded(&s_empty[slot], (use - 1) & 1, A.status);
-        if (free_slot) {
+        if (use > 0 && !mbar_wait_bounded(&s_empty[slot], (use - 1) & 1, A.status)) break;
+        const int phys = (w0.y >= 0 && w0.y < p.num_pages) ? w0.y : -1;
         SlotInfo info;
         info.unit = u;
-        info.lp = lp;
-        info.phys = ok ? phys : -1;
+        info.lp = w0.x;
+        info.phys = phys;
         info.pad = 0;
         info.mask[0] = w1.x; info.mask[1] = w1.y; info.mask[2] = w1.z; info.mask[3] = w1.w;
         s_info[slot] = info;
-        if (ok) {
-          uint8_t* dst = s_tiles + slot * kTileBytes;
-          const int row = (phys * p.Hk + kvh) * kP;
+        if (phys >= 0) {
+          uint8_t* dst = s_tiles + (size_t)slot * kTileBytes;
+          const int row = (phys * p.Hk + (u % p.Hk)) * kP;
           mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
           tma_load_2d(dst, &tmK, 0, row, &s_full[slot]);
           tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_full[slot]);
@@ -325,9 +329,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         } else {
           mbar_arrive(&s_full[slot]);
         }
-        }
       }
-      __syncwarp();
     }
     return;
   }
@@ -364,14 +366,14 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 
     const int ib = (int)(sb - lo), ie = (int)(se - lo);
     for (int i = ib + ((warp - ib % kConsWarps) + kConsWarps) % kConsWarps; i < ie; i += kConsWarps) {
-      // i % kConsWarps == warp, and kSlots % kConsWarps == 0, so the previous use of
+      // i % kConsWarps == warp, and nslots % kConsWarps == 0, so the previous use of
       // this slot was consumed by this same warp: a parity wait cannot alias
-      const int slot = i % kSlots, use = i / kSlots;
+      const int slot = i % nslots, use = i / nslots;
       const bool ok = mbar_wait_bounded(&s_full[slot], use & 1, A.status);
       if (!ok) mbar_wait_bounded(&s_full[slot], use & 1, A.status);   // give a late copy a chance to land
-      const SlotInfo info = s_info[slot];
-      if (ok && info.phys >= 0) {
-        const uint32_t sK = smem_u32(s_tiles + slot * kTileBytes);
+      const SlotInfo* info = s_info + slot;
+      if (ok && info->phys >= 0) {
+        const uint32_t sK = smem_u32(s_tiles + (size_t)slot * kTileBytes);
         const uint32_t sV = sK + kSlab;
         // S = K Q^T  (rows = tokens, cols = heads), two accumulators to halve the chain
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -389,8 +391,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         }
         const float s0 = sa[0] + sb2[0], s1 = sa[1] + sb2[1], s2 = sa[2] + sb2[2], s3 = sa[3] + sb2[3];
         // masks: tokens g4 and g4 + 8, heads 2 t4 and 2 t4 + 1
-        const uint32_t mb0 = (info.mask[g4 >> 2] >> (8 * (g4 & 3))) & 0xffu;
-        const uint32_t mb1 = (info.mask[2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
+        const uint32_t mb0 = (info->mask[g4 >> 2] >> (8 * (g4 & 3))) & 0xffu;
+        const uint32_t mb1 = (info->mask[2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
         const int h0 = 2 * t4, h1 = 2 * t4 + 1;
         const bool v00 = (mb0 >> h0) & 1u, v01 = (mb0 >> h1) & 1u;
         const bool v10 = (mb1 >> h0) & 1u, v11 = (mb1 >> h1) & 1u;
@@ -418,7 +420,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
           o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
         }
         if (A.logits != nullptr) {
-          const int base_tok = info.lp * kP;
+          const int base_tok = info->lp * kP;
           const size_t hs = (size_t)p.mpp * kP;
           const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
           if (v00) A.logits[row0 + h0 * hs + base_tok + g4] = s0 * p.scale;
@@ -465,18 +467,23 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     }
     // ---- merge the consumer warps' states: s_w[warp][head][kPart]
     {
-      float* ww = s_w + warp * 8 * kPart;
+      float* ww = s_w + warp * G * kPart;
+      const bool w0ok = 2 * t4 < G, w1ok = 2 * t4 + 1 < G;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int d = mt * 16 + g4;
-        ww[(2 * t4) * kPart + d] = o[mt][0];
-        ww[(2 * t4 + 1) * kPart + d] = o[mt][1];
-        ww[(2 * t4) * kPart + d + 8] = o[mt][2];
-        ww[(2 * t4 + 1) * kPart + d + 8] = o[mt][3];
+        if (w0ok) {
+          ww[(2 * t4) * kPart + d] = o[mt][0];
+          ww[(2 * t4) * kPart + d + 8] = o[mt][2];
+        }
+        if (w1ok) {
+          ww[(2 * t4 + 1) * kPart + d] = o[mt][1];
+          ww[(2 * t4 + 1) * kPart + d + 8] = o[mt][3];
+        }
       }
       if (g4 == 0) {
-        ww[(2 * t4) * kPart + kD] = m0; ww[(2 * t4 + 1) * kPart + kD] = m1;
-        ww[(2 * t4) * kPart + kD + 1] = l0; ww[(2 * t4 + 1) * kPart + kD + 1] = l1;
+        if (w0ok) { ww[(2 * t4) * kPart + kD] = m0; ww[(2 * t4) * kPart + kD + 1] = l0; }
+        if (w1ok) { ww[(2 * t4 + 1) * kPart + kD] = m1; ww[(2 * t4 + 1) * kPart + kD + 1] = l1; }
       }
     }
     consumer_sync();
@@ -486,15 +493,15 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     for (int g = 0; g < G; ++g) {
       float M = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kConsWarps; ++ww) M = fmaxf(M, s_w[(ww * 8 + g) * kPart + kD]);
+      for (int ww = 0; ww < kConsWarps; ++ww) M = fmaxf(M, s_w[(ww * G + g) * kPart + kD]);
       float acc = 0.f, l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int ww = 0; ww < kConsWarps; ++ww) {
-          const float mw = s_w[(ww * 8 + g) * kPart + kD];
+          const float mw = s_w[(ww * G + g) * kPart + kD];
           const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-          acc += f * s_w[(ww * 8 + g) * kPart + tc];
-          l += f * s_w[(ww * 8 + g) * kPart + kD + 1];
+          acc += f * s_w[(ww * G + g) * kPart + tc];
+          l += f * s_w[(ww * G + g) * kPart + kD + 1];
         }
       }
       if (whole) {
@@ -548,24 +555,37 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   }
 }
 
-size_t decode_smem_bytes(int U) {
-  return 1024 + (size_t)kSlots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * 8 * kPart * 4 +
-         kSlots * sizeof(SlotInfo) + 2 * kSlots * 8 + 32 * 4 + (size_t)(U + 1) * 4;
+size_t decode_smem_bytes_n(int U, int G, int nslots) {
+  return 1024 + (size_t)nslots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * G * kPart * 4 +
+         nslots * sizeof(SlotInfo) + 2 * nslots * 8 + 32 * 4 + (size_t)(U + 1) * 4;
 }
+
+// Slot count: the largest multiple of kConsWarps (<= 16) that still lets two
+// CTAs share an SM; at least kConsWarps.
+int decode_slots(int U, int G) {
+  const size_t per_sm = 228 * 1024, reserve = 1024;
+  int best = kConsWarps;
+  for (int n = kConsWarps; n <= 16; n += kConsWarps)
+    if (2 * (decode_smem_bytes_n(U, G, n) + reserve) <= per_sm) best = n;
+  return best;
+}
+
+size_t decode_smem_bytes(int U) { return decode_smem_bytes_n(U, kMaxG, kConsWarps); }
 
 size_t decode_partials_bytes(const Params& p) { return (size_t)kMaxCtas * 2 * p.G * kPart * sizeof(float); }
 
 size_t tiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * p.mpp * sizeof(Tile); }
 
-int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream) {
+int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
+                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
+                       cudaStream_t stream) {
   const size_t smem = (size_t)p.mpp * sizeof(int);
   if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(build_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.Hk, p.B);
-  build_tiles_kernel<<<grid, kBuildThreads, smem, stream>>>(p, seq_lens, sel_idx, sel_cnt, gran,
-                                                            static_cast<Tile*>(tiles), ntiles, out, lse);
+  build_tiles_kernel<<<grid, kBuildThreads, smem, stream>>>(p, seq_lens, page_table, sel_idx, sel_cnt, gran,
+                                                            static_cast<Tile*>(tiles), ntiles, out, lse, status);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -573,7 +593,8 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
   const int U = p.B * p.Hk;
-  const size_t smem = decode_smem_bytes(U);
+  const int nslots = decode_slots(U, p.G);
+  const size_t smem = decode_smem_bytes_n(U, p.G, nslots);
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int per_sm = 0;
@@ -592,7 +613,7 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.lse = lse;
   A.logits = logits;
   A.status = status;
-  decode_kernel<<<grid, kDecThreads, smem, stream>>>(p, A, tmK, tmV);
+  decode_kernel<<<grid, kDecThreads, smem, stream>>>(p, A, tmK, tmV, nslots);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -24,8 +24,9 @@
 #include "sa_common.cuh"
 
 namespace sa {
-int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream);
+int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
+                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
+                       cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
@@ -123,8 +124,8 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   // what must start at zero: the status word and the split-K arrival counters
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   if (cudaMemsetAsync(counters, 0, (size_t)p.B * p.Hk * sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
-  rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
-                              reinterpret_cast<int*>(b + l.ntiles), out, lse, s);
+  rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
+                              reinterpret_cast<int*>(b + l.ntiles), out, lse, status, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
                            reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,

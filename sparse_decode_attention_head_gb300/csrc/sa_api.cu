@@ -19,8 +19,9 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream);
 size_t topk_smem_bytes(const Params& p);
-int launch_build_tiles(const Params& p, const int* seq_lens, const int* sel_idx, const int* sel_cnt, int gran,
-                       void* tiles, int* ntiles, float* out, float* lse, cudaStream_t stream);
+int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
+                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
+                       cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
@@ -264,8 +265,8 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   if ((rc = make_kv_map(&tmV, v_pool, p)) != SA_OK) return rc;
   const Layout l = layout_of(p);
   cudaStream_t s = as_stream(stream);
-  rc = sa::launch_build_tiles(p, seq_lens, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
-                              at<int>(ws, l.ntiles), out, lse, s);
+  rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
+                              at<int>(ws, l.ntiles), out, lse, at<int>(ws, l.header), s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
                            at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
