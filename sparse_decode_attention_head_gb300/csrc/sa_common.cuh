@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/sa.h"
+#include "sa.h"
 
 namespace sa {
 
