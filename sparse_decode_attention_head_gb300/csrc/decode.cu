@@ -527,26 +527,68 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       consumer_sync();
       if (s_misc[0]) {
         __threadfence();
-        for (int g = 0; g < G; ++g) {
-          float M = -INFINITY;
-          for (int cc = c_first; cc <= c_last; ++cc) {
+        // Merge the CTAs' partials in CTA order.  The (max, sum) of every
+        // (partial, head) is staged in shared memory (s_w is free here) so
+        // the loads overlap instead of forming a dependent chain.
+        const int np = c_last - c_first + 1;
+        const int chunk = 256 / G;            // partials per staging round (2 x 256 floats fit s_w)
+        float* sm_a = s_w;                    // [chunk][G]: max, then weight
+        float* sm_b = s_w + 256;              // [chunk][G]: sum
+        float* sm_M = reinterpret_cast<float*>(s_misc + 8);   // [G]: running max
+        if (tc < G) sm_M[tc] = -INFINITY;
+        consumer_sync();
+        for (int base = 0; base < np; base += chunk) {
+          const int nb = min(np - base, chunk);
+          for (int idx = tc; idx < nb * G; idx += kConsWarps * 32) {
+            const int cc = c_first + base + idx / G, g = idx % G;
             const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
-            M = fmaxf(M, __ldcg(A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart + kD));
+            sm_a[idx] = __ldcg(A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart + kD);
           }
-          float acc = 0.f, l = 0.f;
-          if (M != -INFINITY) {
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
-              const float* pc = A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart;
-              const float mc = __ldcg(pc + kD);
-              const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-              acc += f * __ldcg(pc + tc);
-              l += f * __ldcg(pc + kD + 1);
+          consumer_sync();
+          if (tc < G) {
+            float M = sm_M[tc];
+            for (int j = 0; j < nb; ++j) M = fmaxf(M, sm_a[j * G + tc]);
+            sm_M[tc] = M;
+          }
+          consumer_sync();
+        }
+        float accs[kMaxG], ls[kMaxG];
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) { accs[g] = 0.f; ls[g] = 0.f; }
+        for (int base = 0; base < np; base += chunk) {
+          const int nb = min(np - base, chunk);
+          for (int idx = tc; idx < nb * G; idx += kConsWarps * 32) {
+            const int cc = c_first + base + idx / G, g = idx % G;
+            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
+            const float* pc = A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart;
+            const float mc = __ldcg(pc + kD), M = sm_M[g];
+            sm_a[idx] = (mc == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mc - M);
+            sm_b[idx] = __ldcg(pc + kD + 1);
+          }
+          consumer_sync();
+#pragma unroll 4
+          for (int j = 0; j < nb; ++j) {
+            const int cc = c_first + base + j;
+            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
+            const float* pc = A.partials + ((size_t)cc * 2 + ps) * G * kPart;
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g) {
+              if (g < G) {
+                const float f = sm_a[j * G + g];
+                accs[g] += f * __ldcg(pc + g * kPart + tc);
+                ls[g] += f * sm_b[j * G + g];
+              }
             }
           }
-          const size_t row = (size_t)b * p.Hq + kvh * G + g;
-          A.out[row * kD + tc] = l > 0.f ? acc / l : 0.f;
-          if (tc == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          consumer_sync();
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) {
+          if (g < G) {
+            const size_t row = (size_t)b * p.Hq + kvh * G + g;
+            A.out[row * kD + tc] = ls[g] > 0.f ? accs[g] / ls[g] : 0.f;
+            if (tc == 0) A.lse[row] = ls[g] > 0.f ? (sm_M[g] + log2f(ls[g])) * 0.6931471805599453f : -INFINITY;
+          }
         }
         if (tc == 0) A.counters[u] = 0;
       }
