@@ -298,18 +298,24 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 
   // ------------------------------------------------------------ producer warp
   // Lane j owns slot j and the tiles j, j + nslots, ... of the slice, so every
-  // slot's uses are issued in order by one thread and the lanes run freely.
+  // slot's uses are issued in order by one thread.  The lanes poll their
+  // "empty" barriers with the non-blocking test in one converged loop, so no
+  // lane's wait holds back the others.
   if (warp == kConsWarps) {
-    if (lane < nslots) {
-      const int slot = lane;
-      int u = unit_of(s_prefix, U, lo + lane < hi ? lo + lane : lo);
-      for (int i = lane, use = 0; i < n_local; i += nslots, ++use) {
-        const long long t = lo + i;
-        while (t >= s_prefix[u + 1]) ++u;
-        const Tile* tp = A.tiles + (size_t)u * p.mpp + (t - s_prefix[u]);
-        const int4 w0 = __ldg(reinterpret_cast<const int4*>(tp));       // issued before the wait below
-        const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
-        if (use > 0 && !mbar_wait_bounded(&s_empty[slot], (use - 1) & 1, A.status)) break;
+    int i = lane, use = 0;
+    bool active = lane < nslots && i < n_local;
+    const int slot = lane;
+    int u = unit_of(s_prefix, U, lo + (active ? i : 0));
+    int4 w0 = make_int4(0, 0, 0, 0);
+    uint4 w1 = make_uint4(0, 0, 0, 0);
+    if (active) {
+      const Tile* tp = A.tiles + (size_t)u * p.mpp + (lo + i - s_prefix[u]);
+      w0 = __ldg(reinterpret_cast<const int4*>(tp));
+      w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
+    }
+    uint32_t spins = 0;
+    while (__any_sync(0xffffffffu, active)) {
+      if (active && (use == 0 || mbar_test_wait(&s_empty[slot], (use - 1) & 1))) {
         const int phys = (w0.y >= 0 && w0.y < p.num_pages) ? w0.y : -1;
         SlotInfo info;
         info.unit = u;
@@ -329,6 +335,20 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         } else {
           mbar_arrive(&s_full[slot]);
         }
+        i += nslots;
+        ++use;
+        active = i < n_local;
+        if (active) {   // prefetch the next descriptor; it is used at the next issue
+          const long long t = lo + i;
+          while (t >= s_prefix[u + 1]) ++u;
+          const Tile* tp = A.tiles + (size_t)u * p.mpp + (t - s_prefix[u]);
+          w0 = __ldg(reinterpret_cast<const int4*>(tp));
+          w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
+        }
+      }
+      if (++spins > (1u << 28)) {   // bounded: consumers stopped releasing slots
+        set_status(A.status, SA_ERR_TIMEOUT);
+        break;
       }
     }
     return;
