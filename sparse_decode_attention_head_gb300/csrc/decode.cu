@@ -313,28 +313,6 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       w0 = __ldg(reinterpret_cast<const int4*>(tp));
       w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
     }
-    // L2 prefetch of the lane's later tiles: the descriptor of the next tile to
-    // prefetch is loaded one issue earlier, so the prefetch never waits on it
-    auto pf_page = [&](int j, int& uu) -> int2 {   // (phys, kvh) of slice tile j, or phys -1
-      const long long t = lo + j;
-      while (t >= s_prefix[uu + 1]) ++uu;
-      const int ph = __ldg(&A.tiles[(size_t)uu * p.mpp + (t - s_prefix[uu])].phys);
-      return make_int2(ph, uu % p.Hk);
-    };
-    auto pf_issue = [&](int2 pg) {
-      if (pg.x >= 0 && pg.x < p.num_pages) {
-        const int row = (pg.x * p.Hk + pg.y) * kP;
-        tma_prefetch_2d(&tmK, 0, row);
-        tma_prefetch_2d(&tmK, 64, row);
-        tma_prefetch_2d(&tmV, 0, row);
-        tma_prefetch_2d(&tmV, 64, row);
-      }
-    };
-    int pf_j = lane + nslots, u_pf = u;
-    int2 pf_pg = make_int2(-1, 0);
-    if (lane < nslots && pf_j < n_local) pf_issue(pf_page(pf_j, u_pf));   // warm-up: the lane's second tile
-    pf_j += nslots;
-    if (lane < nslots && pf_j < n_local) pf_pg = pf_page(pf_j, u_pf);
     uint32_t spins = 0;
     while (__any_sync(0xffffffffu, active)) {
       if (active && (use == 0 || mbar_test_wait(&s_empty[slot], (use - 1) & 1))) {
@@ -356,11 +334,6 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
           tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_full[slot]);
         } else {
           mbar_arrive(&s_full[slot]);
-        }
-        if (pf_j < n_local) {   // prefetch two rounds ahead, then load the next target's page
-          pf_issue(pf_pg);
-          pf_j += nslots;
-          if (pf_j < n_local) pf_pg = pf_page(pf_j, u_pf);
         }
         i += nslots;
         ++use;
