@@ -296,3 +296,74 @@ def decode_head(q32, kseq, vseq, L, S, W, Bs, sel_blocks, scale):
     O_J, lse_J = attend(q32, kseq, vseq, J, scale)
     O, lse = lse_merge(O_I, lse_I, O_J, lse_J)
     return dict(O=O, lse=float(lse), O_I=O_I, lse_I=lse_I, O_J=O_J, lse_J=lse_J, I=I, J=J)
+
+
+# ---------------------------------------------------------------------------
+# step a7: vertical / slash score tables (reading R6)
+# ---------------------------------------------------------------------------
+#
+# LFPS ("What carries the argument", Eq. (10)): per head, a table indexed by
+# absolute key position (vertical) and one indexed by offset from the newest
+# token (slash), both decayed by r = 0.95 every step and fed with the step's
+# attention weights; HGCA's moving average of attention weights is the
+# vertical table.  LFPS Eq. (9): candidates are expanded by offsets
+# {-1, 0, 1, 2}.  HGCA: an entry is kept when its average exceeds
+# beta / (number of densely attended entries).
+
+DECAY = 0.95
+EXPANSION_OFFSETS = (-1, 0, 1, 2)
+
+
+def merged_weights(q, kseq, L: int, S: int, W: int, cand_tokens, scale: float):
+    """Attended positions (I plus the candidate tokens inside M, ascending)
+    and their merged softmax weights a_i = exp(z_i - lse), fp64."""
+    s_end, w_beg = partition(L, S, W)
+    J = sorted(set(int(t) for t in cand_tokens if s_end <= t < w_beg))
+    pos = np.array(sorted(set(dense_tokens(L, S, W).tolist()) | set(J)), dtype=np.int64)
+    if len(pos) == 0:
+        return pos, np.zeros(0)
+    z = attention_logits(q, kseq, pos, scale)
+    m = z.max()
+    lse = m + math.log(np.exp(z - m).sum())
+    return pos, np.exp(z - lse)
+
+
+def table_update(vert, slash, L_prev: int, att_pos, att_w, r: float = DECAY):
+    """One decay-and-add step, fp64: T <- r T + (1 - r) a, with a the weight
+    of the entry at the step of length L_prev (0 where not attended).
+    Vertical entry i holds position i; slash entry d holds position
+    L_prev - 1 - d."""
+    n = len(vert)
+    a_pos = np.zeros(n)
+    att_pos = np.asarray(att_pos, dtype=np.int64)
+    a_pos[att_pos] = att_w
+    v_new = r * np.asarray(vert, dtype=F64) + (1.0 - r) * a_pos
+    d = np.arange(n)
+    src = L_prev - 1 - d
+    a_sl = np.where((src >= 0) & (src < n), a_pos[np.clip(src, 0, n - 1)], 0.0)
+    s_new = r * np.asarray(slash, dtype=F64) + (1.0 - r) * a_sl
+    return v_new, s_new
+
+
+def table_candidates(vert32, slash32, L: int, S: int, W: int, beta: float, kcap: int):
+    """Candidate tokens for a step of length L from fp32 tables: seeds i in M
+    with vert[i] > tau or slash[L - 1 - i] > tau (tau = fp32(beta) / fp32(|I|),
+    compared in fp32), expanded by {-1, 0, 1, 2} and clipped to M; ascending.
+    Returns (positions, overflowed): at most kcap, lowest positions kept."""
+    vert32 = np.asarray(vert32, dtype=F32)
+    slash32 = np.asarray(slash32, dtype=F32)
+    s_end, w_beg = partition(L, S, W)
+    n_dense = s_end + (L - w_beg)
+    if w_beg <= s_end or n_dense == 0:
+        return np.zeros(0, dtype=np.int64), False
+    tau = F32(beta) / F32(n_dense)
+    i = np.arange(s_end, w_beg)
+    seed = (vert32[i] > tau) | (slash32[L - 1 - i] > tau)
+    seeds = i[seed]
+    cand = set()
+    for o in EXPANSION_OFFSETS:
+        for j in (seeds + o).tolist():
+            if s_end <= j < w_beg:
+                cand.add(j)
+    out = np.array(sorted(cand), dtype=np.int64)
+    return out[:kcap], len(out) > kcap
