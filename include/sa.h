@@ -191,6 +191,37 @@ int sa_sparse_decode(const sa_problem* prob, const void* q,
                      int32_t sel_granularity, float* out, float* lse,
                      float* logits_or_null, void* ws, void* stream);
 
+/* Step a7 -- score-table update and table-driven candidate selection.
+ * Tables: vertical (entry i = absolute position i) and slash (entry d =
+ * offset d from the newest token, i.e. position L - 1 - d), fp32
+ * [B][Hq][max_pages_per_seq * P], one row per query head.  They are
+ * double-buffered: *_in is read, *_out written; out must not overlap in.
+ * Update (when prev_logits != NULL): with the previous decode step of length
+ * Lp = prev_seq_lens[b] (attended set = its dense set plus the sorted token
+ * list prev_sel_idx[b][h][0..prev_sel_cnt) inside its middle region, logits
+ * and lse as written by sa_sparse_decode), every entry becomes
+ *   T_out = fma(decay, T_in, (1 - decay) * exp(z - lse))   (attended)
+ *   T_out = decay * T_in                                 (not attended)
+ * in fp32; the slash entry d takes the weight of position Lp - 1 - d.
+ * Without prev_logits the tables are copied unchanged.
+ * Selection for the next step of length L = seq_lens[b]: position i in the
+ * middle region M of L is a seed if vert_out[i] > tau or slash_out[L-1-i] >
+ * tau, tau = beta / |I(L)| (fp32, strict); candidates are the seeds expanded
+ * by offsets {-1, 0, 1, 2} and clipped to M, written ascending to
+ * cand_idx[b][h][0..kcap) with cand_cnt[b][h]; beyond kcap the lowest are
+ * kept and SA_ERR_CAPACITY is recorded in the workspace status word.
+ * (LFPS: "What carries the argument", Eq. (9), Eq. (10), r = 0.95; HGCA:
+ * moving average of attention weights and its beta / N threshold.) */
+int sa_update_score_tables(const sa_problem* prob, const float* vert_in,
+                           const float* slash_in, float* vert_out,
+                           float* slash_out, const int32_t* prev_seq_lens,
+                           const int32_t* prev_sel_idx,
+                           const int32_t* prev_sel_cnt,
+                           const float* prev_logits, const float* prev_lse,
+                           const int32_t* seq_lens, float decay, float beta,
+                           int32_t* cand_idx, int32_t* cand_cnt, void* ws,
+                           void* stream);
+
 /* Sparse decode without a workspace.  The pages have no counterpart to this
  * call; it exists for callers that cannot allocate device memory and so
  * cannot hand sa_sparse_decode a workspace -- for example code running inside

@@ -30,6 +30,24 @@ size_t decode_partials_bytes(const Params& p);
 size_t tiles_bytes(const Params& p);
 int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                      const float* lse_b, float* o, float* lse, cudaStream_t stream);
+struct TableArgs {
+  const float* vin;
+  const float* sin;
+  float* vout;
+  float* sout;
+  const int* prev_lens;
+  const int* prev_sel;
+  const int* prev_cnt;
+  const float* prev_logits;
+  const float* prev_lse;
+  const int* lens;
+  int* cand;
+  int* cand_cnt;
+  int* status;
+  float decay;
+  float beta;
+};
+int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -271,6 +289,48 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
                            at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
                            at<int>(ws, l.header), tmK, tmV, nsm, s);
+}
+
+int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const float* slash_in, float* vert_out,
+                           float* slash_out, const int32_t* prev_seq_lens, const int32_t* prev_sel_idx,
+                           const int32_t* prev_sel_cnt, const float* prev_logits, const float* prev_lse,
+                           const int32_t* seq_lens, float decay, float beta, int32_t* cand_idx, int32_t* cand_cnt,
+                           void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!vert_in || !slash_in || !vert_out || !slash_out || !seq_lens || !cand_idx || !cand_cnt || !ws)
+    return SA_ERR_INVALID_ARG;
+  if (!(decay > 0.f && decay < 1.f) || !(beta > 0.f) || !std::isfinite(beta)) return SA_ERR_INVALID_ARG;
+  const bool has_prev = prev_logits != nullptr;
+  if (has_prev && (!prev_seq_lens || !prev_sel_idx || !prev_sel_cnt || !prev_lse)) return SA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)p.B * p.Hq * p.mpp * SA_PAGE_SIZE * sizeof(float);
+  auto overlap = [bytes](const void* a, const void* b) {
+    const char* x = static_cast<const char*>(a);
+    const char* y = static_cast<const char*>(b);
+    return x < y + bytes && y < x + bytes;
+  };
+  if (overlap(vert_out, vert_in) || overlap(vert_out, slash_in) || overlap(slash_out, vert_in) ||
+      overlap(slash_out, slash_in) || overlap(vert_out, slash_out))
+    return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  sa::TableArgs A;
+  A.vin = vert_in;
+  A.sin = slash_in;
+  A.vout = vert_out;
+  A.sout = slash_out;
+  A.prev_lens = prev_seq_lens;
+  A.prev_sel = prev_sel_idx;
+  A.prev_cnt = prev_sel_cnt;
+  A.prev_logits = prev_logits;
+  A.prev_lse = prev_lse;
+  A.lens = seq_lens;
+  A.cand = cand_idx;
+  A.cand_cnt = cand_cnt;
+  A.status = at<int>(ws, l.header);
+  A.decay = decay;
+  A.beta = beta;
+  return sa::launch_tables(p, A, as_stream(stream));
 }
 
 int sa_lse_merge(int32_t n_rows, int32_t D, const float* o_a, const float* lse_a, const float* o_b,

@@ -76,6 +76,8 @@ def lib():
             "sa_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_lse_merge": (ctypes.c_int, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
+            "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                      ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -238,3 +240,27 @@ def lse_merge(o_a, lse_a, o_b, lse_b, o, lse):
         _need(t, torch.float32, nm, (n,))
     _check(lib().sa_lse_merge(n, D, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse),
                               _stream()), "sa_lse_merge")
+
+
+def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, seq_lens, cand_idx, cand_cnt,
+                        ws: Workspace, decay: float = 0.95, beta: float = 1.0, prev=None):
+    """prev: None (first step: tables copied) or a dict with prev_seq_lens,
+    prev_sel_idx, prev_sel_cnt, prev_logits, prev_lse of the previous step."""
+    N = prob.max_pages_per_seq * prob.page_size
+    for t, nm in ((vert_in, "vert_in"), (slash_in, "slash_in"), (vert_out, "vert_out"), (slash_out, "slash_out")):
+        _need(t, torch.float32, nm, (prob.B, prob.Hq, N))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    _need(cand_idx, torch.int32, "cand_idx", (prob.B, prob.Hq, prob.kcap))
+    _need(cand_cnt, torch.int32, "cand_cnt", (prob.B, prob.Hq))
+    pv = prev or {}
+    if prev is not None:
+        _need(pv["prev_seq_lens"], torch.int32, "prev_seq_lens", (prob.B,))
+        _need(pv["prev_sel_idx"], torch.int32, "prev_sel_idx", (prob.B, prob.Hq, prob.kcap))
+        _need(pv["prev_sel_cnt"], torch.int32, "prev_sel_cnt", (prob.B, prob.Hq))
+        _need(pv["prev_logits"], torch.float32, "prev_logits", (prob.B, prob.Hq, N))
+        _need(pv["prev_lse"], torch.float32, "prev_lse", (prob.B, prob.Hq))
+    _check(lib().sa_update_score_tables(
+        prob.ref, _ptr(vert_in), _ptr(slash_in), _ptr(vert_out), _ptr(slash_out), _ptr(pv.get("prev_seq_lens")),
+        _ptr(pv.get("prev_sel_idx")), _ptr(pv.get("prev_sel_cnt")), _ptr(pv.get("prev_logits")),
+        _ptr(pv.get("prev_lse")), _ptr(seq_lens), decay, beta, _ptr(cand_idx), _ptr(cand_cnt), _ptr(ws.buf),
+        _stream()), "sa_update_score_tables")

@@ -201,3 +201,118 @@ def make_decode_case(wl: Workload, seed: int, device="cpu") -> DecodeCase:
     return DecodeCase(wl=wl, q=q_bf, k_pool=k_pool.to(torch.bfloat16),
                       v_pool=v_pool.to(torch.bfloat16), page_table=page_table,
                       seq_lens=seq_lens, g_hat=g_hat, heavy=heavy_all)
+
+
+# --------------------------------------------------------------------------
+# score-table workloads (table-driven selection over consecutive steps)
+# --------------------------------------------------------------------------
+
+@dataclass
+class TableWorkload:
+    """Consecutive decode steps whose candidates come from the score tables.
+
+    Planted structure (a reading of the "drifting planted heavy positions" of
+    the workload): per (sequence, KV group) n_vert heavy absolute positions in
+    the middle region, one replaced every `drift` steps, plus heavy offsets
+    from the newest token; each step's query leans on the keys there."""
+
+    name: str
+    B: int
+    Hq: int
+    Hk: int
+    L0: int                         # tokens at the first step (current token included)
+    steps: int
+    S: int = 4
+    W: int = 1024
+    kcap: int = 6554
+    beta: float = 1.0
+    n_vert: int = 8
+    slash_offsets: tuple = (2000, 5000, 20000, 60000)
+    drift: int = 8
+    c_q: float = 1.5
+    t0_heavy: float = 0.02          # initial table value at planted entries
+    t0_noise: float = 1e-5          # scale of the initial table elsewhere
+    D: int = HEAD_DIM
+    P: int = PAGE_SIZE
+
+    @property
+    def G(self):
+        return self.Hq // self.Hk
+
+    @property
+    def max_pages_per_seq(self):
+        return (self.L0 + self.steps + self.P - 1) // self.P
+
+
+def table_workload(name: str) -> TableWorkload:
+    if name == "tables_128k":
+        # Llama-3-8B shape, batch 4, 131072 tokens growing by one per step
+        return TableWorkload(name, B=4, Hq=32, Hk=8, L0=131072, steps=64)
+    if name == "tables_small":
+        return TableWorkload(name, B=2, Hq=8, Hk=2, L0=8192, steps=16, W=256, kcap=512, n_vert=4,
+                             slash_offsets=(300, 1000, 4000, 7000), drift=4)
+    raise KeyError(name)
+
+
+@dataclass
+class TableCase:
+    wl: TableWorkload
+    k_pool: torch.Tensor        # bf16 [num_pages, Hk, P, D]
+    v_pool: torch.Tensor
+    page_table: torch.Tensor    # int32 [B, max_pages]
+    q_steps: torch.Tensor       # bf16 [steps, B, Hq, D]
+    vert0: torch.Tensor         # fp32 [B, Hq, max_pages * P]
+    slash0: torch.Tensor
+    heavy: list                 # [step][b][kvh] -> positions
+
+
+def make_table_case(wl: TableWorkload, seed: int, device="cpu") -> TableCase:
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    B, Hq, Hk, G, D, P = wl.B, wl.Hq, wl.Hk, wl.G, wl.D, wl.P
+    mpp = wl.max_pages_per_seq
+    num_pages = B * mpp
+    k_pool = torch.randn(num_pages, Hk, P, D, generator=g, device=dev).to(torch.bfloat16)
+    v_pool = torch.randn(num_pages, Hk, P, D, generator=g, device=dev).to(torch.bfloat16)
+    page_table = torch.randperm(num_pages, generator=g, device=dev).reshape(B, mpp).to(torch.int32)
+    N = mpp * P
+    lo_m, hi_m = wl.S, wl.L0 - wl.W
+    heavy0 = torch.randint(lo_m, hi_m, (B, Hk, wl.n_vert), generator=g, device=dev)
+    repl = torch.randint(lo_m, hi_m, (wl.steps // max(1, wl.drift) + 1, B, Hk), generator=g, device=dev)
+    z = torch.randn(wl.steps, B, Hq, D, generator=g, device=dev)
+    noise_v = torch.rand(B, Hq, N, generator=g, device=dev) * wl.t0_noise
+    noise_s = torch.rand(B, Hq, N, generator=g, device=dev) * wl.t0_noise
+
+    def key(b, kvh, pos):   # fp32 key rows of logical positions pos [n]
+        pg = page_table[b, pos // P].long()
+        return k_pool[pg, kvh, pos % P].float()
+
+    heavy_steps = []
+    cur = heavy0.clone()
+    q = torch.empty(wl.steps, B, Hq, D, device=dev)
+    for t in range(wl.steps):
+        if t > 0 and wl.drift > 0 and t % wl.drift == 0:
+            cur[:, :, (t // wl.drift - 1) % wl.n_vert] = repl[t // wl.drift]
+        heavy_steps.append(cur.clone())
+        L = wl.L0 + t
+        for b in range(B):
+            for kvh in range(Hk):
+                pos_v = cur[b, kvh]
+                pos_s = torch.tensor([L - 1 - d for d in wl.slash_offsets if L - 1 - d >= 0], device=dev)
+                kk = torch.cat([key(b, kvh, pos_v), key(b, kvh, pos_s)])
+                khat = kk / kk.norm(dim=-1, keepdim=True) * math.sqrt(D)
+                lean = wl.c_q * khat.sum(dim=0)
+                q[t, b, kvh * G:(kvh + 1) * G] = z[t, b, kvh * G:(kvh + 1) * G] + lean
+    vert0 = noise_v.clone()
+    slash0 = noise_s.clone()
+    vert0[:, :, wl.L0:] = 0.0
+    slash0[:, :, wl.L0:] = 0.0
+    for b in range(B):
+        for h in range(Hq):
+            vert0[b, h, heavy0[b, h // G]] += wl.t0_heavy
+            for d in wl.slash_offsets:
+                if d < wl.L0:
+                    slash0[b, h, d] += wl.t0_heavy
+    return TableCase(wl=wl, k_pool=k_pool, v_pool=v_pool, page_table=page_table,
+                     q_steps=q.to(torch.bfloat16), vert0=vert0.contiguous(), slash0=slash0.contiguous(),
+                     heavy=[h.tolist() for h in heavy_steps])
