@@ -33,8 +33,6 @@ def _run(wl, seed, nsteps, heads=None):
     cand = [torch.zeros(B, Hq, wl.kcap, dtype=torch.int32, device="cuda") for _ in range(2)]
     cnt = [torch.zeros(B, Hq, dtype=torch.int32, device="cuda") for _ in range(2)]
     logits = torch.zeros(B, Hq, N, device="cuda")
-    out = torch.empty(B, Hq, 128, device="cuda")
-    lse = torch.empty(B, Hq, device="cuda")
     heads = heads or [(b, h) for b in range(B) for h in range(Hq)]
     prev = None
     prev_L = None
@@ -86,7 +84,7 @@ def _run(wl, seed, nsteps, heads=None):
             H.assert_close(o_np[b, h], O_ref, f"step {t} O")
             H.assert_close(np.array([l_np[b, h]]), np.array([float(lse_ref)]), f"step {t} lse")
         prev = dict(prev_seq_lens=seq_lens, prev_sel_idx=cand[cur], prev_sel_cnt=cnt[cur], prev_logits=logits,
-                    prev_lse=lse)
+                    prev_lse=l)
         prev_c, prev_n, prev_L = c_gpu, n_gpu, L
     return n_cands
 
