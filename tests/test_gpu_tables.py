@@ -95,9 +95,10 @@ def test_tables_small_all_steps():
     assert min(n) > 0   # the planted entries keep producing candidates
 
 
-def test_tables_128k_llama_shape_first_steps():
-    # the 131072-token, batch-4 Llama-shaped workload at full size, sampled heads
+def test_tables_128k_llama_shape_64_steps():
+    # the 131072-token, batch-4 Llama-shaped workload at full size over all 64
+    # steps (the GPU runs every head; the oracle checks a sample of heads)
     wl = synth.table_workload("tables_128k")
     heads = [(0, 0), (1, 9), (2, 17), (3, 31)]
-    n = _run(wl, 3, 6, heads=heads)
+    n = _run(wl, 3, wl.steps, heads=heads)
     assert min(n) > 0
