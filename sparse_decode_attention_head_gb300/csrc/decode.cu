@@ -44,7 +44,7 @@ struct __align__(16) Tile {
   uint32_t mask[4];  // byte i = G-bit mask of heads attending token 16 lp + i
 };
 
-constexpr int kBuildThreads = 512;
+constexpr int kBuildThreads = 1024;
 constexpr int kConsWarps = 4;                      // consumer warps
 constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
 constexpr int kMaxCtas = 1024;                     // grid cap (partial slots are sized for it)
@@ -131,29 +131,41 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
   const int total = scan_tmp[nw - 1];
   const uint32_t all = (1u << G) - 1u;
   for (int i = a; i < e; ++i) {
-    if (flag[i]) {
-      // dense-set tokens of this page attend for every head
-      Tile t;
-      t.lp = i;
-      const int phys = __ldg(page_table + (size_t)b * p.mpp + i);
-      const bool ok = phys >= 0 && phys < p.num_pages;
-      if (!ok) set_status(status, SA_ERR_BAD_PAGE);
-      t.phys = ok ? phys : -1;
-      t.pad[0] = t.pad[1] = 0;
+    if (flag[i]) flag[i] = base++;
+    else flag[i] = -1;
+  }
+  __syncthreads();
+  // descriptors: page-table loads of 4 pages are in flight together
+  for (int i0 = tid; i0 < npg; i0 += 4 * blockDim.x) {
+    int ph[4];
 #pragma unroll
-      for (int w4 = 0; w4 < 4; ++w4) {
-        uint32_t m = 0;
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + k * blockDim.x;
+      ph[k] = (i < npg && flag[i] >= 0) ? __ldg(page_table + (size_t)b * p.mpp + i) : 0;
+    }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int tok = i * kP + 4 * w4 + r;
-          if (tok < Lc && (tok < s_end || tok >= w_beg)) m |= all << (8 * r);
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + k * blockDim.x;
+      if (i < npg && flag[i] >= 0) {
+        Tile t;
+        t.lp = i;
+        const bool ok = ph[k] >= 0 && ph[k] < p.num_pages;
+        if (!ok) set_status(status, SA_ERR_BAD_PAGE);
+        t.phys = ok ? ph[k] : -1;
+        t.pad[0] = t.pad[1] = 0;
+        // dense-set tokens of this page attend for every head
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int tok = i * kP + 4 * w4 + r;
+            if (tok < Lc && (tok < s_end || tok >= w_beg)) m |= all << (8 * r);
+          }
+          t.mask[w4] = m;
         }
-        t.mask[w4] = m;
+        T[flag[i]] = t;
       }
-      T[base] = t;
-      flag[i] = base++;
-    } else {
-      flag[i] = -1;
     }
   }
   __syncthreads();

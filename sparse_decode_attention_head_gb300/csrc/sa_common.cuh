@@ -34,7 +34,7 @@ struct WsHeader {
 };
 
 __device__ __forceinline__ void set_status(int* status, int code) {
-  atomicCAS(status, SA_OK, code);
+  if (status != nullptr) atomicCAS(status, SA_OK, code);
 }
 
 // Dense set I = [0, s_end) U [w_beg, L), middle region M = [s_end, w_beg).
@@ -118,6 +118,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
   set_status(status, SA_ERR_TIMEOUT);
   return false;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 2-D tiled TMA load of one box into shared memory, completion on `bar`.

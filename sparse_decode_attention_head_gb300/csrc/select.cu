@@ -26,6 +26,9 @@ template <int G, int MODE>
 __global__ void __launch_bounds__(kScoreWarps * 32)
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
              const int* __restrict__ seq_lens, float* __restrict__ scores, int always) {
+  // the CTA's candidate summaries are contiguous: one bulk copy stages them
+  extern __shared__ __align__(128) uint8_t s_sum[];   // kScoreBlocksPerCta x row bytes
+  __shared__ uint64_t s_bar;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int L = min(seq_lens[b], p.mpp * kP);
   const int Bs = p.bs[kvh];
@@ -38,6 +41,17 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 #pragma unroll
   for (int g = 0; g < G; ++g) all_dense &= (p.k[kvh * G + g] >= ncand);
   if (all_dense && !always) return;  // every head keeps every candidate: no ranking needed
+
+  constexpr int kRowElems = (MODE == SA_SUMMARY_MINMAX) ? 2 * kD : kD;
+  constexpr int kRowBytes = kRowElems * 2;
+  const int nb = min(kScoreBlocksPerCta, ncand - cta_first);
+  const size_t unit_slot = ((size_t)b * p.Hk + kvh) * p.slots;
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&s_bar, nb * kRowBytes);
+    bulk_load_1d(s_sum, summ + (unit_slot + j0 + cta_first) * kRowElems, nb * kRowBytes, &s_bar);
+  }
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3;   // block within the warp's group of 4
@@ -60,32 +74,36 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
       selw[g][i] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
     }
   }
+  __syncthreads();   // barrier initialised before anyone waits on it
+  if (!mbar_wait_bounded(&s_bar, 0, nullptr)) return;
 
-  const size_t unit_slot = ((size_t)b * p.Hk + kvh) * p.slots;
-  const int warp_first = cta_first + warp * 4 * kScoreIters;
+  // lanes 4..7 of a block read their two 16-byte halves in swapped order, so
+  // the 8 lanes of a quarter-warp hit 8 distinct bank groups
+  const int hf = (part >> 2) & 1;
+  const int warp_first = warp * 4 * kScoreIters;
 #pragma unroll
   for (int it = 0; it < kScoreIters; ++it) {
-    const int c = warp_first + it * 4 + sub;
-    const bool valid = c < ncand;
-    const int j = j0 + (valid ? c : 0);
+    const int cl = warp_first + it * 4 + sub;     // block within the CTA's chunk
+    const bool valid = cl < nb;
+    const int c = cta_first + cl;
+    const uint4* base = reinterpret_cast<const uint4*>(s_sum + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
     uint32_t xmin[8], xmax[8];
+    uint4 lo0, lo1;
+    {
+      const uint4 f = base[hf], s2 = base[hf ^ 1];
+      lo0 = hf ? s2 : f;
+      lo1 = hf ? f : s2;
+    }
     if (MODE == SA_SUMMARY_MINMAX) {
-      const uint4* base = reinterpret_cast<const uint4*>(summ + (unit_slot + j) * 2 * kD + 16 * part);
-      uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
-      if (valid) {
-        a0 = __ldg(base); a1 = __ldg(base + 1);                    // min, dims 16 part ..
-        b0 = __ldg(base + kD / 8); b1 = __ldg(base + kD / 8 + 1);  // max
-      }
-      xmin[0] = a0.x; xmin[1] = a0.y; xmin[2] = a0.z; xmin[3] = a0.w;
-      xmin[4] = a1.x; xmin[5] = a1.y; xmin[6] = a1.z; xmin[7] = a1.w;
-      xmax[0] = b0.x; xmax[1] = b0.y; xmax[2] = b0.z; xmax[3] = b0.w;
-      xmax[4] = b1.x; xmax[5] = b1.y; xmax[6] = b1.z; xmax[7] = b1.w;
+      const uint4 f = base[kD / 8 + hf], s2 = base[kD / 8 + (hf ^ 1)];
+      const uint4 hi0 = hf ? s2 : f, hi1 = hf ? f : s2;
+      xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
+      xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
+      xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
+      xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
     } else {
-      const uint4* base = reinterpret_cast<const uint4*>(summ + (unit_slot + j) * kD + 16 * part);
-      uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
-      if (valid) { a0 = __ldg(base); a1 = __ldg(base + 1); }
-      xmax[0] = a0.x; xmax[1] = a0.y; xmax[2] = a0.z; xmax[3] = a0.w;
-      xmax[4] = a1.x; xmax[5] = a1.y; xmax[6] = a1.z; xmax[7] = a1.w;
+      xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
+      xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
 #pragma unroll
       for (int i = 0; i < 8; ++i) xmin[i] = 0u;
     }
@@ -108,7 +126,7 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
       acc = __fadd_rn(acc, 0.0f);
       if (part == g) my_score = acc;
     }
-    if (valid && part < G) scores[((size_t)b * p.Hq + kvh * G + part) * p.slots + j] = my_score;
+    if (valid && part < G) scores[((size_t)b * p.Hq + kvh * G + part) * p.slots + j0 + c] = my_score;
   }
 }
 
@@ -188,9 +206,18 @@ topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ 
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-      const uint32_t u = keys[i];
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    // warp-aggregated: one atomic per distinct digit per warp (in the top
+    // passes nearly all keys share a digit)
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + tid;
+      const uint32_t u = i < n ? keys[i] : 0u;
+      const bool take = i < n && (u & mask) == prefix;
+      const uint32_t digit = (u >> shift) & 255u;
+      const unsigned act = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        const unsigned peers = __match_any_sync(act, digit);
+        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+      }
     }
     __syncthreads();
     if (tid < 32) {
@@ -259,14 +286,18 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   dim3 grid((p.slots + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta, p.Hk, p.B);
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* sb = static_cast<const __nv_bfloat16*>(summ);
-#define SA_SCORE_CASE(GG)                                                                     \
-  case GG:                                                                                    \
-    if (p.mode == SA_SUMMARY_MINMAX)                                                          \
-      score_kernel<GG, SA_SUMMARY_MINMAX>                                                     \
-          <<<grid, kScoreWarps * 32, 0, stream>>>(p, qb, sb, seq_lens, scores, always);       \
-    else                                                                                      \
-      score_kernel<GG, SA_SUMMARY_MEAN>                                                       \
-          <<<grid, kScoreWarps * 32, 0, stream>>>(p, qb, sb, seq_lens, scores, always);       \
+  const size_t smem_mm = (size_t)kScoreBlocksPerCta * 2 * kD * 2, smem_mean = smem_mm / 2;
+#define SA_SCORE_CASE(GG)                                                                          \
+  case GG:                                                                                         \
+    if (p.mode == SA_SUMMARY_MINMAX) {                                                             \
+      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MINMAX>,                                    \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_mm);             \
+      score_kernel<GG, SA_SUMMARY_MINMAX>                                                          \
+          <<<grid, kScoreWarps * 32, smem_mm, stream>>>(p, qb, sb, seq_lens, scores, always);      \
+    } else {                                                                                       \
+      score_kernel<GG, SA_SUMMARY_MEAN>                                                            \
+          <<<grid, kScoreWarps * 32, smem_mean, stream>>>(p, qb, sb, seq_lens, scores, always);    \
+    }                                                                                              \
     break;
   switch (p.G) {
     SA_SCORE_CASE(1)
