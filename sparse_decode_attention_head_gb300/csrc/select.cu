@@ -23,7 +23,7 @@ constexpr int kScoreIters = 4;                                     // 4 blocks p
 constexpr int kScoreBlocksPerCta = kScoreWarps * 4 * kScoreIters;  // 128
 
 template <int G, int MODE>
-__global__ void __launch_bounds__(kScoreWarps * 32, 2)
+__global__ void __launch_bounds__(kScoreWarps * 32, (G <= 4 ? 2 : 1))
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
              const int* __restrict__ seq_lens, float* __restrict__ scores, int always) {
   // the CTA's candidate summaries are contiguous: one bulk copy stages them
