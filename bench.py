@@ -98,7 +98,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -208,26 +208,43 @@ def run_ours(args):
     assert ws.status() == sa.SA_OK
     nbytes = [algorithmic_bytes(wl, prob, L["sl"].cpu().numpy(), L["sel_idx"], L["sel_cnt"]) for L in layers]
 
-    # one CUDA graph per (layer, sub-step): the timed loop only replays
+    # The timed work is captured once into CUDA graphs holding all K steps, so
+    # the GPU runs them back to back whatever the host's launch rate:
+    #   g_step: K whole steps (select + decode), layers rotating;
+    #   g_dec / g_sel: the K decode calls / the K select calls alone, for the
+    #   per-kernel averages the roofline uses.
+    K, W = args.steps, args.warmup
     stream = torch.cuda.Stream(device=dev)
-    g_sel, g_dec = [], []
-    with torch.cuda.stream(stream):
-        for L in layers:
-            g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g1, stream=stream, capture_error_mode="relaxed"):
-                sub_select(L)
-            with torch.cuda.graph(g2, stream=stream, capture_error_mode="relaxed"):
-                sub_decode(L)
-            g_sel.append(g1)
-            g_dec.append(g2)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for i in range(K):
+                    fn(layers[(W + i) % N_LAYERS])
+        return g
+
+    g_step = capture(lambda L: (sub_select(L), sub_decode(L)))
+    g_dec = capture(sub_decode)
+    g_sel = capture(sub_select)
     torch.cuda.synchronize()
 
-    K, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    with torch.cuda.stream(stream):
+    def timed(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    with torch.cuda.stream(stream):   # warm-up steps, eager
         for i in range(W):
-            g_sel[i % N_LAYERS].replay()
-            g_dec[i % N_LAYERS].replay()
+            sub_select(layers[i % N_LAYERS])
+            sub_decode(layers[i % N_LAYERS])
+    timed(g_dec)                      # first replays upload the graphs
+    timed(g_sel)
+    timed(g_step)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -235,19 +252,12 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            l = (W + i) % N_LAYERS
-            ev[i][0].record(stream)
-            g_sel[l].replay()
-            ev[i][1].record(stream)
-            g_dec[l].replay()
-            ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    total_ms = timed(g_step)
+    dec_total = timed(g_dec)
+    sel_total = timed(g_sel)
     clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    sel_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [dec_total / K]
+    sel_ms = [sel_total / K]
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=dev)
@@ -400,7 +410,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
