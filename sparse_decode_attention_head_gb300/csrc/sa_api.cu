@@ -15,7 +15,7 @@ namespace sa {
 int launch_summarize(const Params& p, const void* k_pool, const int* page_table, const int* seq_lens,
                      int block_begin, int block_end, void* summ, int* status, cudaStream_t stream);
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
-                 int always, cudaStream_t stream);
+                 int always, int num_sms, cudaStream_t stream);
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream);
 size_t topk_smem_bytes(const Params& p);
@@ -244,7 +244,9 @@ int sa_score_blocks(const sa_problem* prob, const void* q, const void* summaries
   if (rc != SA_OK) return rc;
   if (!q || !summaries || !seq_lens || !scores || !ws) return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
-  return sa::launch_score(p, q, summaries, seq_lens, scores, 1, as_stream(stream));
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SA_ERR_CUDA;
+  return sa::launch_score(p, q, summaries, seq_lens, scores, 1, nsm, as_stream(stream));
 }
 
 int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries, const int32_t* seq_lens,
@@ -258,7 +260,9 @@ int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries,
   const Layout l = layout_of(p);
   float* scores = scores_or_null ? scores_or_null : at<float>(ws, l.scores);
   cudaStream_t s = as_stream(stream);
-  rc = sa::launch_score(p, q, summaries, seq_lens, scores, scores_or_null != nullptr, s);
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SA_ERR_CUDA;
+  rc = sa::launch_score(p, q, summaries, seq_lens, scores, scores_or_null != nullptr, nsm, s);
   if (rc != SA_OK) return rc;
   return sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s);
 }

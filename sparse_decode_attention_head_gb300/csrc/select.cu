@@ -14,290 +14,330 @@
 // MSB-first radix select over order-preserving uint32 keys finds the k-th
 // key T and how many keys equal to T to take; a stable block-wide
 // compaction then emits the chosen indices in ascending order.
+#include <algorithm>
+
 #include "sa_common.cuh"
 
 namespace sa {
 
-constexpr int kScoreWarps = 8;
-constexpr int kScoreIters = 4;                                     // 4 blocks per warp per iteration
-constexpr int kScoreBlocksPerCta = kScoreWarps * 4 * kScoreIters;  // 128
+constexpr int kScoreWarps = 8;                 // consumer warps (+1 producer warp)
+constexpr int kItemBlocks = 64;                // candidate blocks per work item (8 per consumer warp)
+constexpr int kMaxUnitsScore = 4096;
 
+// Work items are (unit = (b, kv head), run of kItemBlocks candidate blocks).
+// Each CTA takes a contiguous range of items; a producer thread streams each
+// item's summaries (contiguous) and the group's q into a ring of shared-memory
+// stages with 1-D bulk copies; consumer warps score the staged blocks.
 template <int G, int MODE>
-__global__ void __launch_bounds__(kScoreWarps * 32, (G <= 4 ? 2 : 1))
+__global__ void __launch_bounds__((kScoreWarps + 1) * 32, 1)
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
-             const int* __restrict__ seq_lens, float* __restrict__ scores, int always) {
-  // the CTA's candidate summaries are contiguous: one bulk copy stages them
-  extern __shared__ __align__(128) uint8_t s_sum[];   // kScoreBlocksPerCta x row bytes
-  __shared__ uint64_t s_bar;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int L = min(seq_lens[b], p.mpp * kP);
-  const int Bs = p.bs[kvh];
-  int j0, j1;
-  candidate_range(L, p.S, p.W, Bs, j0, j1);
-  const int ncand = j1 - j0;
-  const int cta_first = blockIdx.x * kScoreBlocksPerCta;
-  if (cta_first >= ncand) return;
-  bool all_dense = true;
-#pragma unroll
-  for (int g = 0; g < G; ++g) all_dense &= (p.k[kvh * G + g] >= ncand);
-  if (all_dense && !always) return;  // every head keeps every candidate: no ranking needed
-
+             const int* __restrict__ seq_lens, float* __restrict__ scores, int always, int nstages) {
   constexpr int kRowElems = (MODE == SA_SUMMARY_MINMAX) ? 2 * kD : kD;
   constexpr int kRowBytes = kRowElems * 2;
-  const int nb = min(kScoreBlocksPerCta, ncand - cta_first);
-  const size_t unit_slot = ((size_t)b * p.Hk + kvh) * p.slots;
-  if (threadIdx.x == 0) {
-    mbar_init(&s_bar, 1);
+  constexpr int kStageBytes = kItemBlocks * kRowBytes + kMaxG * kD * 2;   // summaries + q
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t s_full[16], s_empty[16];
+  __shared__ int s_items[kMaxUnitsScore + 1];   // prefix of items over units
+
+  const int U = p.B * p.Hk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // items per unit (0 when every head keeps every candidate and scores are not asked for)
+  for (int u = tid; u < U; u += blockDim.x) {
+    const int b = u / p.Hk, kvh = u % p.Hk;
+    const int L = min(seq_lens[b], p.mpp * kP);
+    int j0, j1;
+    candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+    const int ncand = j1 - j0;
+    bool all_dense = true;
+    for (int g = 0; g < G; ++g) all_dense &= (p.k[kvh * G + g] >= ncand);
+    s_items[u + 1] = (all_dense && !always) ? 0 : (ncand + kItemBlocks - 1) / kItemBlocks;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < nstages; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kScoreWarps);
+    }
     fence_mbar_init();
-    mbar_arrive_expect_tx(&s_bar, nb * kRowBytes);
-    bulk_load_1d(s_sum, summ + (unit_slot + j0 + cta_first) * kRowElems, nb * kRowBytes, &s_bar);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    s_items[0] = 0;
+    for (int u = 0; u < U; ++u) s_items[u + 1] += s_items[u];
+  }
+  __syncthreads();
+  const long long total = s_items[U];
+  const long long it_lo = total * blockIdx.x / gridDim.x, it_hi = total * (blockIdx.x + 1) / gridDim.x;
+  const int n_items = (int)(it_hi - it_lo);
+  if (n_items <= 0) return;
+
+  auto unit_of = [&](long long it) {
+    int lo = 0, hi = U;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_items[mid] <= it) lo = mid; else hi = mid;
+    }
+    return lo;
+  };
+
+  if (warp == kScoreWarps) {   // ---------------- producer
+    if (lane == 0) {
+      int u = unit_of(it_lo);
+      for (int i = 0; i < n_items; ++i) {
+        const long long it = it_lo + i;
+        while (it >= s_items[u + 1]) ++u;
+        const int b = u / p.Hk, kvh = u % p.Hk;
+        const int L = min(seq_lens[b], p.mpp * kP);
+        int j0, j1;
+        candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+        const int first = (int)(it - s_items[u]) * kItemBlocks;
+        const int nb = min(kItemBlocks, (j1 - j0) - first);
+        const int st = i % nstages, use = i / nstages;
+        if (use > 0 && !mbar_wait_bounded(&s_empty[st], (use - 1) & 1, nullptr)) break;
+        uint8_t* dst = smem + (size_t)st * kStageBytes;
+        mbar_arrive_expect_tx(&s_full[st], nb * kRowBytes + G * kD * 2);
+        bulk_load_1d(dst, summ + ((((size_t)b * p.Hk + kvh) * p.slots) + j0 + first) * kRowElems, nb * kRowBytes,
+                     &s_full[st]);
+        bulk_load_1d(dst + kItemBlocks * kRowBytes, q + ((size_t)b * p.Hq + kvh * G) * kD, G * kD * 2, &s_full[st]);
+      }
+    }
+    return;
   }
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // ---------------- consumers
   const int sub = lane >> 3;   // block within the warp's group of 4
   const int part = lane & 7;   // dims [16 part, 16 part + 16)
-
-  // q of the G heads, this lane's 16 dims, fp32 (exact from bf16)
+  const int hf = (part >> 2) & 1;   // lanes 4..7 read their halves swapped: no bank conflicts
   float qf[G][16];
-  uint32_t selw[G][8];   // byte-permute selectors: take max where q >= 0, else min
+  uint32_t selw[G][8];
+  int cur_unit = -1;
+  int u = unit_of(it_lo);
+  for (int i = 0; i < n_items; ++i) {
+    const long long it = it_lo + i;
+    while (it >= s_items[u + 1]) ++u;
+    const int b = u / p.Hk, kvh = u % p.Hk;
+    const int L = min(seq_lens[b], p.mpp * kP);
+    int j0, j1;
+    candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+    const int first = (int)(it - s_items[u]) * kItemBlocks;
+    const int nb = min(kItemBlocks, (j1 - j0) - first);
+    const int st = i % nstages, use = i / nstages;
+    if (!mbar_wait_bounded(&s_full[st], use & 1, nullptr)) break;
+    const uint8_t* stage = smem + (size_t)st * kStageBytes;
+    if (u != cur_unit) {   // q of the G heads, this lane's 16 dims, fp32 (exact from bf16)
+      cur_unit = u;
+      const uint4* qs = reinterpret_cast<const uint4*>(stage + kItemBlocks * kRowBytes);
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * p.Hq + kvh * G + g) * kD + 16 * part);
-    const uint4 a = __ldg(src), c = __ldg(src + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      for (int g = 0; g < G; ++g) {
+        const uint4 a = qs[g * (kD / 8) + 2 * part], c = qs[g * (kD / 8) + 2 * part + 1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      qf[g][2 * i] = bf16_lo(w[i]);
-      qf[g][2 * i + 1] = bf16_hi(w[i]);
-      const bool p0 = qf[g][2 * i] >= 0.f, p1 = qf[g][2 * i + 1] >= 0.f;
-      // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
-      selw[g][i] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
-    }
-  }
-  __syncthreads();   // barrier initialised before anyone waits on it
-  if (!mbar_wait_bounded(&s_bar, 0, nullptr)) return;
-
-  // lanes 4..7 of a block read their two 16-byte halves in swapped order, so
-  // the 8 lanes of a quarter-warp hit 8 distinct bank groups
-  const int hf = (part >> 2) & 1;
-  const int warp_first = warp * 4 * kScoreIters;
-#pragma unroll
-  for (int it = 0; it < kScoreIters; ++it) {
-    const int cl = warp_first + it * 4 + sub;     // block within the CTA's chunk
-    const bool valid = cl < nb;
-    const int c = cta_first + cl;
-    const uint4* base = reinterpret_cast<const uint4*>(s_sum + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
-    uint32_t xmin[8], xmax[8];
-    uint4 lo0, lo1;
-    {
-      const uint4 f = base[hf], s2 = base[hf ^ 1];
-      lo0 = hf ? s2 : f;
-      lo1 = hf ? f : s2;
-    }
-    if (MODE == SA_SUMMARY_MINMAX) {
-      const uint4 f = base[kD / 8 + hf], s2 = base[kD / 8 + (hf ^ 1)];
-      const uint4 hi0 = hf ? s2 : f, hi1 = hf ? f : s2;
-      xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
-      xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
-      xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
-      xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
-    } else {
-      xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
-      xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xmin[i] = 0u;
-    }
-    float my_score = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[i], xmin[i], selw[g][i]) : xmax[i];
-        if (i == 0)
-          acc = __fmul_rn(qf[g][0], bf16_lo(w));
-        else
-          acc = __fmaf_rn(qf[g][2 * i], bf16_lo(w), acc);
-        acc = __fmaf_rn(qf[g][2 * i + 1], bf16_hi(w), acc);
+        for (int k2 = 0; k2 < 8; ++k2) {
+          qf[g][2 * k2] = bf16_lo(w[k2]);
+          qf[g][2 * k2 + 1] = bf16_hi(w[k2]);
+          const bool p0 = qf[g][2 * k2] >= 0.f, p1 = qf[g][2 * k2 + 1] >= 0.f;
+          // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
+          selw[g][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
+        }
       }
-      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
-      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
-      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-      acc = __fadd_rn(acc, 0.0f);
-      if (part == g) my_score = acc;
     }
-    if (valid && part < G) scores[((size_t)b * p.Hq + kvh * G + part) * p.slots + j0 + c] = my_score;
+#pragma unroll
+    for (int r = 0; r < kItemBlocks / (4 * kScoreWarps); ++r) {
+      const int cl = (r * kScoreWarps + warp) * 4 + sub;   // block within the item
+      const bool valid = cl < nb;
+      const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
+      uint32_t xmin[8], xmax[8];
+      uint4 lo0, lo1;
+      {
+        const uint4 f = base[hf], s2 = base[hf ^ 1];
+        lo0 = hf ? s2 : f;
+        lo1 = hf ? f : s2;
+      }
+      if (MODE == SA_SUMMARY_MINMAX) {
+        const uint4 f = base[kD / 8 + hf], s2 = base[kD / 8 + (hf ^ 1)];
+        const uint4 hi0 = hf ? s2 : f, hi1 = hf ? f : s2;
+        xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
+        xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
+        xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
+        xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
+      } else {
+        xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
+        xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
+      }
+      float my_score = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+          const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[k2], xmin[k2], selw[g][k2]) : xmax[k2];
+          if (k2 == 0)
+            acc = __fmul_rn(qf[g][0], bf16_lo(w));
+          else
+            acc = __fmaf_rn(qf[g][2 * k2], bf16_lo(w), acc);
+          acc = __fmaf_rn(qf[g][2 * k2 + 1], bf16_hi(w), acc);
+        }
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
+        acc = __fadd_rn(acc, 0.0f);
+        if (part == g) my_score = acc;
+      }
+      if (valid && part < G) scores[((size_t)b * p.Hq + kvh * G + part) * p.slots + j0 + first + cl] = my_score;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[st]);
   }
 }
 
 // ---------------------------------------------------------------- top-k
 
-constexpr int kTopkThreads = 512;
+// One warp selects for one head, so the passes need no block barrier.
+constexpr int kTopkWarpsMax = 4;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one int per thread; returns the prefix and
-// writes the total to *total.  Uses `tmp` (>= 32 ints of shared memory).
-__device__ __forceinline__ int block_excl_scan(int v, int* tmp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  int x = v;
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? tmp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < nw) tmp[lane] = w;  // inclusive warp totals
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
-  *total = tmp[nw - 1];
-  __syncthreads();
-  return before;
+  return x;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
-            int* __restrict__ sel_idx, int* __restrict__ sel_cnt) {
-  extern __shared__ uint32_t keys[];
-  __shared__ int hist[256];
-  __shared__ int scan_tmp[32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_krem;
-
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int kvh = h / p.G;
-  const int L = min(seq_lens[b], p.mpp * kP);
-  const int Bs = p.bs[kvh];
-  int j0, j1;
-  candidate_range(L, p.S, p.W, Bs, j0, j1);
-  const int n = j1 - j0;
-  const int k = min(p.k[h], n);
-  int* out = sel_idx + ((size_t)b * p.Hq + h) * p.kcap;
-  const int tid = threadIdx.x;
-
-  if (k >= n) {  // keep every candidate (100 % budget, or no candidates); n <= k <= kcap
-    for (int i = tid; i < n; i += blockDim.x) out[i] = j0 + i;
-    if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = n;
-    return;
-  }
-  if (k <= 0) {
-    if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = 0;
-    return;
-  }
-
-  const float* sc = scores + ((size_t)b * p.Hq + h) * p.slots + j0;
-  for (int i = tid; i < n; i += blockDim.x) keys[i] = order_key(sc[i]);
-
+// Warp-collective: the k largest of keys[0, n) by (key desc, index asc),
+// 0 < k < n, written ascending as base_idx + i to out[0, k).  `hist` is 256
+// ints of this warp's shared memory.  MSB-first radix select in 4 passes of 8
+// bits with warp-aggregated histogram updates, then a stable compaction in
+// index order (each lane owns a contiguous index range).
+__device__ void warp_topk(const uint32_t* keys, int n, int k, int* hist, int base_idx, int* out) {
+  const int lane = threadIdx.x & 31;
   uint32_t prefix = 0, mask = 0;
   int krem = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    // warp-aggregated: one atomic per distinct digit per warp (in the top
-    // passes nearly all keys share a digit)
-    for (int base = 0; base < n; base += blockDim.x) {
-      const int i = base + tid;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) hist[lane * 8 + q] = 0;
+    __syncwarp();
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
       const uint32_t u = i < n ? keys[i] : 0u;
       const bool take = i < n && (u & mask) == prefix;
       const uint32_t digit = (u >> shift) & 255u;
       const unsigned act = __ballot_sync(0xffffffffu, take);
       if (take) {
         const unsigned peers = __match_any_sync(act, digit);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+        if (lane == __ffs(peers) - 1) hist[digit] += __popc(peers);   // one writer per digit per round
       }
+      __syncwarp();
     }
-    __syncthreads();
-    if (tid < 32) {
-      // lane l owns digits 255-8l .. 248-8l (descending)
-      int cnt[8], tot = 0;
+    // lane l owns digits 255-8l .. 248-8l (descending)
+    int cnt[8], tot = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { cnt[i] = hist[255 - 8 * tid - i]; tot += cnt[i]; }
-      int incl = tot;
+    for (int q = 0; q < 8; ++q) { cnt[q] = hist[255 - 8 * lane - q]; tot += cnt[q]; }
+    const int incl = warp_incl_scan(tot);
+    int above = incl - tot;
+    int found_digit = -1, found_krem = 0;
+    if (above < krem && krem <= incl) {
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += y;
-      }
-      int above = incl - tot;
-      if (above < krem && krem <= incl) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above < krem && krem <= above + cnt[i]) {
-            s_prefix = prefix | ((uint32_t)(255 - 8 * tid - i) << shift);
-            s_krem = krem - above;
-          }
-          above += cnt[i];
+      for (int q = 0; q < 8; ++q) {
+        if (found_digit < 0 && above < krem && krem <= above + cnt[q]) {
+          found_digit = 255 - 8 * lane - q;
+          found_krem = krem - above;
         }
+        above += cnt[q];
       }
     }
-    __syncthreads();
-    prefix = s_prefix;
-    krem = s_krem;
+    const unsigned who = __ballot_sync(0xffffffffu, found_digit >= 0);
+    const int src = __ffs(who) - 1;
+    found_digit = __shfl_sync(0xffffffffu, found_digit, src);
+    found_krem = __shfl_sync(0xffffffffu, found_krem, src);
+    prefix |= (uint32_t)found_digit << shift;
     mask |= 255u << shift;
+    krem = found_krem;
+    __syncwarp();
   }
   const uint32_t T = prefix;   // key of the k-th best
-  const int need_eq = krem;    // how many keys equal to T are taken (lowest index first)
+  const int need_eq = krem;    // keys equal to T that are taken, lowest index first
+  const int per = (n + 31) / 32;
+  const int lo = min(n, lane * per), hi = min(n, lo + per);
+  int eq = 0, gt = 0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t u = keys[i];
+    eq += u == T;
+    gt += u > T;
+  }
+  const int eq_before = warp_incl_scan(eq) - eq;
+  const int take = gt + max(0, min(eq, need_eq - eq_before));
+  int pos = warp_incl_scan(take) - take;
+  int r = eq_before;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t u = keys[i];
+    bool t = u > T;
+    if (u == T) { t = r < need_eq; ++r; }
+    if (t) out[pos++] = base_idx + i;
+  }
+}
 
-  // stable compaction in ascending index order
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int eq = 0;
-  for (int i = lo; i < hi; ++i) eq += (keys[i] == T);
-  int tot;
-  const int eq_before = block_excl_scan(eq, scan_tmp, &tot);
-  int take = 0;
-  {
-    int r = eq_before;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t u = keys[i];
-      if (u > T) ++take;
-      else if (u == T) { if (r < need_eq) ++take; ++r; }
-    }
+__global__ void __launch_bounds__(kTopkWarpsMax * 32)
+topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
+            int* __restrict__ sel_idx, int* __restrict__ sel_cnt, int warps_per_cta) {
+  extern __shared__ uint32_t smem_k[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= warps_per_cta) return;
+  const int gh = blockIdx.x * warps_per_cta + warp;   // global (b, h) index
+  if (gh >= p.B * p.Hq) return;
+  const int b = gh / p.Hq, h = gh % p.Hq;
+  uint32_t* keys = smem_k + (size_t)warp * (p.slots + 256);
+  int* hist = reinterpret_cast<int*>(keys + p.slots);
+  const int kvh = h / p.G;
+  const int L = min(seq_lens[b], p.mpp * kP);
+  int j0, j1;
+  candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+  const int n = j1 - j0;
+  const int k = min(p.k[h], n);
+  int* out = sel_idx + ((size_t)b * p.Hq + h) * p.kcap;
+  if (k >= n || k <= 0) {   // keep every candidate (100 % budget, or none) / keep none
+    const int m = k >= n ? n : 0;
+    for (int i = lane; i < m; i += 32) out[i] = j0 + i;
+    if (lane == 0) sel_cnt[(size_t)b * p.Hq + h] = m;
+    return;
   }
-  const int pos0 = block_excl_scan(take, scan_tmp, &tot);
-  {
-    int r = eq_before, pos = pos0;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t u = keys[i];
-      bool t = false;
-      if (u > T) t = true;
-      else if (u == T) { t = r < need_eq; ++r; }
-      if (t) out[pos++] = j0 + i;
-    }
-  }
-  if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = k;
+  const float* sc = scores + ((size_t)b * p.Hq + h) * p.slots + j0;
+  for (int i = lane; i < n; i += 32) keys[i] = order_key(__ldg(sc + i));
+  __syncwarp();
+  warp_topk(keys, n, k, hist, j0, out);
+  if (lane == 0) sel_cnt[(size_t)b * p.Hq + h] = k;
 }
 
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
-                 int always, cudaStream_t stream) {
-  dim3 grid((p.slots + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta, p.Hk, p.B);
+                 int always, int num_sms, cudaStream_t stream) {
+  if (p.B * p.Hk > kMaxUnitsScore) return SA_ERR_UNSUPPORTED;
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* sb = static_cast<const __nv_bfloat16*>(summ);
-  const size_t smem_mm = (size_t)kScoreBlocksPerCta * 2 * kD * 2, smem_mean = smem_mm / 2;
-#define SA_SCORE_CASE(GG)                                                                          \
-  case GG:                                                                                         \
-    if (p.mode == SA_SUMMARY_MINMAX) {                                                             \
-      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MINMAX>,                                    \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_mm);             \
-      score_kernel<GG, SA_SUMMARY_MINMAX>                                                          \
-          <<<grid, kScoreWarps * 32, smem_mm, stream>>>(p, qb, sb, seq_lens, scores, always);      \
-    } else {                                                                                       \
-      score_kernel<GG, SA_SUMMARY_MEAN>                                                            \
-          <<<grid, kScoreWarps * 32, smem_mean, stream>>>(p, qb, sb, seq_lens, scores, always);    \
-    }                                                                                              \
+  const int row_bytes = (p.mode == SA_SUMMARY_MINMAX ? 2 : 1) * kD * 2;
+  const size_t stage = (size_t)kItemBlocks * row_bytes + kMaxG * kD * 2;
+  const int nstages = (int)std::min<size_t>(16, (200 * 1024) / stage);
+  const size_t smem = stage * nstages;
+  const int grid = std::max(1, num_sms);
+#define SA_SCORE_CASE(GG)                                                                         \
+  case GG:                                                                                        \
+    if (p.mode == SA_SUMMARY_MINMAX) {                                                            \
+      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MINMAX>,                                   \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+      score_kernel<GG, SA_SUMMARY_MINMAX><<<grid, (kScoreWarps + 1) * 32, smem, stream>>>(        \
+          p, qb, sb, seq_lens, scores, always, nstages);                                          \
+    } else {                                                                                      \
+      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MEAN>,                                     \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+      score_kernel<GG, SA_SUMMARY_MEAN><<<grid, (kScoreWarps + 1) * 32, smem, stream>>>(          \
+          p, qb, sb, seq_lens, scores, always, nstages);                                          \
+    }                                                                                             \
     break;
   switch (p.G) {
     SA_SCORE_CASE(1)
@@ -315,16 +355,23 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-size_t topk_smem_bytes(const Params& p) { return (size_t)p.slots * sizeof(uint32_t); }
+static int topk_warps(const Params& p) {
+  const size_t per_warp = ((size_t)p.slots + 256) * sizeof(uint32_t);
+  int w = (int)std::min<size_t>(kTopkWarpsMax, (200 * 1024) / per_warp);
+  return w < 1 ? 1 : w;
+}
+
+size_t topk_smem_bytes(const Params& p) { return ((size_t)p.slots + 256) * sizeof(uint32_t) * topk_warps(p); }
 
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream) {
+  const int w = topk_warps(p);
   const size_t smem = topk_smem_bytes(p);
   if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  dim3 grid(p.Hq, p.B);
-  topk_kernel<<<grid, kTopkThreads, smem, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+  const int heads = p.B * p.Hq;
+  topk_kernel<<<(heads + w - 1) / w, w * 32, smem, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt, w);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
