@@ -211,6 +211,26 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
   return x;
 }
 
+// Block-wide exclusive scan of one int per thread; returns the prefix and
+// writes the total to *total.  `tmp` holds >= blockDim.x / 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int x = warp_incl_scan(v);
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? tmp[lane] : 0;
+    w = warp_incl_scan(w);
+    if (lane < nw) tmp[lane] = w;   // inclusive warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
+  *total = tmp[nw - 1];
+  __syncthreads();
+  return before;
+}
+
 // Warp-collective: the k largest of keys[0, n) by (key desc, index asc),
 // 0 < k < n, written ascending as base_idx + i to out[0, k).  `hist` is 256
 // ints of this warp's shared memory.  MSB-first radix select in 4 passes of 8
@@ -284,17 +304,20 @@ __device__ void warp_topk(const uint32_t* keys, int n, int k, int* hist, int bas
   }
 }
 
-__global__ void __launch_bounds__(kTopkWarpsMax * 32)
+// Block top-k for one (b, head): each thread holds KPT consecutive keys in
+// registers (so the final compaction is already in index order).  The radix
+// passes start below the bits that every key shares (taken from the block's
+// min and max key), so typically 2-3 passes of 8 bits remain.
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT)
 topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
-            int* __restrict__ sel_idx, int* __restrict__ sel_cnt, int warps_per_cta) {
-  extern __shared__ uint32_t smem_k[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= warps_per_cta) return;
-  const int gh = blockIdx.x * warps_per_cta + warp;   // global (b, h) index
-  if (gh >= p.B * p.Hq) return;
-  const int b = gh / p.Hq, h = gh % p.Hq;
-  uint32_t* keys = smem_k + (size_t)warp * (p.slots + 256);
-  int* hist = reinterpret_cast<int*>(keys + p.slots);
+            int* __restrict__ sel_idx, int* __restrict__ sel_cnt) {
+  __shared__ int hist[256];
+  __shared__ int s_red[2][NT / 32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_krem;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int kvh = h / p.G;
   const int L = min(seq_lens[b], p.mpp * kP);
   int j0, j1;
@@ -304,15 +327,103 @@ topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ 
   int* out = sel_idx + ((size_t)b * p.Hq + h) * p.kcap;
   if (k >= n || k <= 0) {   // keep every candidate (100 % budget, or none) / keep none
     const int m = k >= n ? n : 0;
-    for (int i = lane; i < m; i += 32) out[i] = j0 + i;
-    if (lane == 0) sel_cnt[(size_t)b * p.Hq + h] = m;
+    for (int i = tid; i < m; i += NT) out[i] = j0 + i;
+    if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = m;
     return;
   }
   const float* sc = scores + ((size_t)b * p.Hq + h) * p.slots + j0;
-  for (int i = lane; i < n; i += 32) keys[i] = order_key(__ldg(sc + i));
-  __syncwarp();
-  warp_topk(keys, n, k, hist, j0, out);
-  if (lane == 0) sel_cnt[(size_t)b * p.Hq + h] = k;
+  uint32_t key[KPT];
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tid * KPT + q;
+    key[q] = i < n ? order_key(__ldg(sc + i)) : 0u;
+    if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
+  }
+  // block min / max -> the bits all keys share
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) { s_red[0][warp] = (int)kmin; s_red[1][warp] = (int)kmax; }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0xffffffffu, c = 0u;
+    for (int w = 0; w < NT / 32; ++w) { a = min(a, (uint32_t)s_red[0][w]); c = max(c, (uint32_t)s_red[1][w]); }
+    s_prefix = a;        // temporarily: min
+    s_krem = (int)c;     // temporarily: max
+  }
+  __syncthreads();
+  const uint32_t gmin = s_prefix, gmax = (uint32_t)s_krem;
+  const int common = gmin == gmax ? 32 : __clz(gmin ^ gmax);   // leading bits shared by every key
+  uint32_t mask = common >= 32 ? 0xffffffffu : (common == 0 ? 0u : (0xffffffffu << (32 - common)));
+  uint32_t prefix = gmin & mask;
+  int krem = k;
+  __syncthreads();
+  for (int top = 32 - common; top > 0; top -= 8) {   // bits [top-8, top) are this pass's digit
+    const int shift = max(0, top - 8);
+    const uint32_t dmask = (1u << (top - shift)) - 1u;
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = tid * KPT + q;
+      if (i < n && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & dmask], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l .. 248-8l (descending)
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { cnt[q] = hist[255 - 8 * lane - q]; tot += cnt[q]; }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int above = incl - tot;
+      if (above < krem && krem <= incl) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (above < krem && krem <= above + cnt[q]) {
+            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
+            s_krem = krem - above;
+          }
+          above += cnt[q];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    krem = s_krem;
+    mask |= dmask << shift;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;   // key of the k-th best (all 32 bits resolved)
+  const int need_eq = krem;    // keys equal to T that are taken, lowest index first
+  int eq = 0, gt = 0;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tid * KPT + q;
+    if (i < n) { eq += key[q] == T; gt += key[q] > T; }
+  }
+  int total;
+  const int eq_before = block_excl_scan(eq, &s_red[0][0], &total);
+  const int take = gt + max(0, min(eq, need_eq - eq_before));
+  int pos = block_excl_scan(take, &s_red[1][0], &total);
+  int r = eq_before;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tid * KPT + q;
+    if (i < n) {
+      bool t = key[q] > T;
+      if (key[q] == T) { t = r < need_eq; ++r; }
+      if (t) out[pos++] = j0 + i;
+    }
+  }
+  if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = k;
 }
 
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
@@ -355,23 +466,22 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-static int topk_warps(const Params& p) {
-  const size_t per_warp = ((size_t)p.slots + 256) * sizeof(uint32_t);
-  int w = (int)std::min<size_t>(kTopkWarpsMax, (200 * 1024) / per_warp);
-  return w < 1 ? 1 : w;
-}
-
-size_t topk_smem_bytes(const Params& p) { return ((size_t)p.slots + 256) * sizeof(uint32_t) * topk_warps(p); }
+size_t topk_smem_bytes(const Params&) { return 0; }
 
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream) {
-  const int w = topk_warps(p);
-  const size_t smem = topk_smem_bytes(p);
-  if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  const int heads = p.B * p.Hq;
-  topk_kernel<<<(heads + w - 1) / w, w * 32, smem, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt, w);
+  dim3 grid(p.Hq, p.B);
+  // the largest candidate count any head can have
+  int max_n = 0;
+  for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  if (max_n <= 256 * 8)
+    topk_kernel<256, 8><<<grid, 256, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+  else if (max_n <= 1024 * 16)
+    topk_kernel<1024, 16><<<grid, 1024, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+  else if (max_n <= 1024 * 64)
+    topk_kernel<1024, 64><<<grid, 1024, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+  else
+    return SA_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
