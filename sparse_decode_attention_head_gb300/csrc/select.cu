@@ -106,7 +106,6 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   // ---------------- consumers
   const int sub = lane >> 3;   // block within the warp's group of 4
   const int part = lane & 7;   // dims [16 part, 16 part + 16)
-  const int hf = (part >> 2) & 1;   // lanes 4..7 read their halves swapped: no bank conflicts
   float qf[G][16];
   uint32_t selw[G][8];
   int cur_unit = -1;
@@ -146,15 +145,9 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
       const bool valid = cl < nb;
       const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
       uint32_t xmin[8], xmax[8];
-      uint4 lo0, lo1;
-      {
-        const uint4 f = base[hf], s2 = base[hf ^ 1];
-        lo0 = hf ? s2 : f;
-        lo1 = hf ? f : s2;
-      }
+      const uint4 lo0 = base[0], lo1 = base[1];
       if (MODE == SA_SUMMARY_MINMAX) {
-        const uint4 f = base[kD / 8 + hf], s2 = base[kD / 8 + (hf ^ 1)];
-        const uint4 hi0 = hf ? s2 : f, hi1 = hf ? f : s2;
+        const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
         xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
         xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
         xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
