@@ -48,6 +48,7 @@ constexpr int kBuildThreads = 1024;
 constexpr int kConsWarps = 4;                      // consumer warps
 constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
 constexpr int kMaxCtas = 1024;                     // grid cap (partial slots are sized for it)
+constexpr int kMaxSlotsPerWarp = 4;                // slots <= 16
 constexpr int kPart = kD + 2;                      // floats per head in a partial: O[kD], max, sum
 constexpr int kSlab = kP * kD * 2;           // 4096 bytes: one page of one KV head
 constexpr int kTileBytes = 2 * kSlab;        // K + V
@@ -275,6 +276,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       mbar_init(&s_empty[i], 1);
     }
     fence_mbar_init();
+    s_misc[16] = 0;
   }
   // prefix over the units' tile counts (block-wide scan)
   {
@@ -309,25 +311,51 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   const int n_local = (int)(hi - lo);
 
   // ------------------------------------------------------------ producer warp
-  // Lane j owns slot j and the tiles j, j + nslots, ... of the slice, so every
-  // slot's uses are issued in order by one thread.  The lanes poll their
-  // "empty" barriers with the non-blocking test in one converged loop, so no
-  // lane's wait holds back the others.
+  // Lane j (< nslots) owns slot j and issues that slot's uses in order.  The
+  // slice's tiles are handed out in order to whichever slots are free, so a
+  // tile that lands late holds back only its own slot.  Descriptors come in
+  // batches of 32 (one per lane, the next batch loaded ahead) and are passed
+  // to the issuing lane by shuffle.
   if (warp == kConsWarps) {
-    int i = lane, use = 0;
-    bool active = lane < nslots && i < n_local;
-    const int slot = lane;
-    int u = unit_of(s_prefix, U, lo + (active ? i : 0));
-    int4 w0 = make_int4(0, 0, 0, 0);
-    uint4 w1 = make_uint4(0, 0, 0, 0);
-    if (active) {
-      const Tile* tp = A.tiles + (size_t)u * p.mpp + (lo + i - s_prefix[u]);
-      w0 = __ldg(reinterpret_cast<const int4*>(tp));
-      w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
-    }
+    const bool owner = lane < nslots;
+    int use = 0, next = 0, dbase = 0;
+    int4 dA0, dB0;
+    uint4 dA1, dB1;
+    auto load_desc = [&](int base_, int4& w0, uint4& w1) {
+      const int i = base_ + lane;
+      if (i < n_local) {
+        const long long t = lo + i;
+        const int uu = unit_of(s_prefix, U, t);
+        const Tile* tp = A.tiles + (size_t)uu * p.mpp + (t - s_prefix[uu]);
+        w0 = __ldg(reinterpret_cast<const int4*>(tp));
+        w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
+        w0.z = uu;   // the unit rides in a pad field
+      } else {
+        w0 = make_int4(0, -1, 0, 0);
+        w1 = make_uint4(0, 0, 0, 0);
+      }
+    };
+    load_desc(0, dA0, dA1);
+    load_desc(32, dB0, dB1);
     uint32_t spins = 0;
-    while (__any_sync(0xffffffffu, active)) {
-      if (active && (use == 0 || mbar_test_wait(&s_empty[slot], (use - 1) & 1))) {
+    while (next < n_local) {
+      const bool free_slot = owner && (use == 0 || mbar_test_wait(&s_empty[lane], (use - 1) & 1));
+      const unsigned fm = __ballot_sync(0xffffffffu, free_slot);
+      const int n_issue = min(__popc(fm), min(32 - (next - dbase), n_local - next));
+      const int rank = __popc(fm & ((1u << lane) - 1u));
+      const bool mine = free_slot && rank < n_issue;
+      const int src = next - dbase + (mine ? rank : 0);
+      int4 w0;
+      uint4 w1;
+      w0.x = __shfl_sync(0xffffffffu, dA0.x, src);
+      w0.y = __shfl_sync(0xffffffffu, dA0.y, src);
+      w0.z = __shfl_sync(0xffffffffu, dA0.z, src);
+      w1.x = __shfl_sync(0xffffffffu, dA1.x, src);
+      w1.y = __shfl_sync(0xffffffffu, dA1.y, src);
+      w1.z = __shfl_sync(0xffffffffu, dA1.z, src);
+      w1.w = __shfl_sync(0xffffffffu, dA1.w, src);
+      if (mine) {
+        const int slot = lane, u = w0.z;
         const int phys = (w0.y >= 0 && w0.y < p.num_pages) ? w0.y : -1;
         SlotInfo info;
         info.unit = u;
@@ -347,18 +375,16 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         } else {
           mbar_arrive(&s_full[slot]);
         }
-        i += nslots;
         ++use;
-        active = i < n_local;
-        if (active) {   // prefetch the next descriptor; it is used at the next issue
-          const long long t = lo + i;
-          while (t >= s_prefix[u + 1]) ++u;
-          const Tile* tp = A.tiles + (size_t)u * p.mpp + (t - s_prefix[u]);
-          w0 = __ldg(reinterpret_cast<const int4*>(tp));
-          w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
-        }
       }
-      if (++spins > (1u << 28)) {   // bounded: consumers stopped releasing slots
+      next += n_issue;
+      if (next - dbase >= 32) {   // move to the next batch and load the one after it
+        dA0 = dB0;
+        dA1 = dB1;
+        dbase += 32;
+        load_desc(dbase + 32, dB0, dB1);
+      }
+      if (n_issue == 0 && ++spins > (1u << 28)) {   // bounded: consumers stopped releasing slots
         set_status(A.status, SA_ERR_TIMEOUT);
         break;
       }
@@ -372,6 +398,9 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   uint8_t* sp = s_p + warp * 512;
   const uint32_t sp_hi = smem_u32(sp), sp_lo = sp_hi + 256;
   const int tc = tid;   // consumer thread index == head-dim index in the merges (kConsWarps * 32 == kD)
+  int uses[kMaxSlotsPerWarp];   // completed uses of each of this warp's slots
+#pragma unroll
+  for (int m = 0; m < kMaxSlotsPerWarp; ++m) uses[m] = 0;
 
   for (int u = unit_of(s_prefix, U, lo); u < U && s_prefix[u] < hi; ++u) {
     const long long ub = s_prefix[u], ue = s_prefix[u + 1];
@@ -396,100 +425,122 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    const int ib = (int)(sb - lo), ie = (int)(se - lo);
-    for (int i = ib + ((warp - ib % kConsWarps) + kConsWarps) % kConsWarps; i < ie; i += kConsWarps) {
-      // i % kConsWarps == warp, and nslots % kConsWarps == 0, so the previous use of
-      // this slot was consumed by this same warp: a parity wait cannot alias
-      const int slot = i % nslots, use = i / nslots;
-      const bool ok = mbar_wait_bounded(&s_full[slot], use & 1, A.status);
-      if (!ok) mbar_wait_bounded(&s_full[slot], use & 1, A.status);   // give a late copy a chance to land
-      const SlotInfo* info = s_info + slot;
-      if (ok && info->phys >= 0) {
-        const uint32_t sK = smem_u32(s_tiles + (size_t)slot * kTileBytes);
-        const uint32_t sV = sK + kSlab;
-        // S = K Q^T  (rows = tokens, cols = heads), two accumulators to halve the chain
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int mi = lane >> 3, r = lane & 7;
-          const int row = (mi & 1) * 8 + r;
+    const int seg_size = (int)(se - sb);
+    // poll this warp's slots (warp, warp + kConsWarps, ...) and take whichever
+    // has landed; a slot holding a later unit's tile is left for its segment
+    bool held[kMaxSlotsPerWarp];
 #pragma unroll
-          for (int ks = 0; ks < 8; ks += 2) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(sK + swz(row, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
-            mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            ldsm_x4(sK + swz(row, (ks + 1) * 2 + (mi >> 1)), a0, a1, a2, a3);
-            mma_bf16_16816(sb2, a0, a1, a2, a3, qb[ks + 1][0], qb[ks + 1][1]);
+    for (int m = 0; m < kMaxSlotsPerWarp; ++m) held[m] = false;
+    uint32_t spins = 0;
+    while (true) {
+#pragma unroll
+      for (int m = 0; m < kMaxSlotsPerWarp; ++m) {
+        const int slot = warp + kConsWarps * m;
+        if (slot >= nslots || held[m]) continue;
+        const bool ready = __shfl_sync(0xffffffffu, (int)mbar_test_wait(&s_full[slot], uses[m] & 1), 0) != 0;
+        if (!ready) continue;
+        const SlotInfo* info = s_info + slot;
+        if (info->unit != u) {
+          held[m] = true;
+          continue;
+        }
+        if (info->phys >= 0) {
+          const uint32_t sK = smem_u32(s_tiles + (size_t)slot * kTileBytes);
+          const uint32_t sV = sK + kSlab;
+          // S = K Q^T  (rows = tokens, cols = heads), two accumulators to halve the chain
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const int mi = lane >> 3, r = lane & 7;
+            const int row = (mi & 1) * 8 + r;
+#pragma unroll
+            for (int ks = 0; ks < 8; ks += 2) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(sK + swz(row, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
+              mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              ldsm_x4(sK + swz(row, (ks + 1) * 2 + (mi >> 1)), a0, a1, a2, a3);
+              mma_bf16_16816(sb2, a0, a1, a2, a3, qb[ks + 1][0], qb[ks + 1][1]);
+            }
           }
-        }
-        const float s0 = sa[0] + sb2[0], s1 = sa[1] + sb2[1], s2 = sa[2] + sb2[2], s3 = sa[3] + sb2[3];
-        // masks: tokens g4 and g4 + 8, heads 2 t4 and 2 t4 + 1
-        const uint32_t mb0 = (info->mask[g4 >> 2] >> (8 * (g4 & 3))) & 0xffu;
-        const uint32_t mb1 = (info->mask[2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
-        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-        const bool v00 = (mb0 >> h0) & 1u, v01 = (mb0 >> h1) & 1u;
-        const bool v10 = (mb1 >> h0) & 1u, v11 = (mb1 >> h1) & 1u;
-        const float z00 = v00 ? s0 * scale_log2 : -INFINITY;
-        const float z01 = v01 ? s1 * scale_log2 : -INFINITY;
-        const float z10 = v10 ? s2 * scale_log2 : -INFINITY;
-        const float z11 = v11 ? s3 * scale_log2 : -INFINITY;
-        float t0 = fmaxf(z00, z10), t1 = fmaxf(z01, z11);
+          const float s0 = sa[0] + sb2[0], s1 = sa[1] + sb2[1], s2 = sa[2] + sb2[2], s3 = sa[3] + sb2[3];
+          // masks: tokens g4 and g4 + 8, heads 2 t4 and 2 t4 + 1
+          const uint32_t mb0 = (info->mask[g4 >> 2] >> (8 * (g4 & 3))) & 0xffu;
+          const uint32_t mb1 = (info->mask[2 + (g4 >> 2)] >> (8 * (g4 & 3))) & 0xffu;
+          const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+          const bool v00 = (mb0 >> h0) & 1u, v01 = (mb0 >> h1) & 1u;
+          const bool v10 = (mb1 >> h0) & 1u, v11 = (mb1 >> h1) & 1u;
+          const float z00 = v00 ? s0 * scale_log2 : -INFINITY;
+          const float z01 = v01 ? s1 * scale_log2 : -INFINITY;
+          const float z10 = v10 ? s2 * scale_log2 : -INFINITY;
+          const float z11 = v11 ? s3 * scale_log2 : -INFINITY;
+          float t0 = fmaxf(z00, z10), t1 = fmaxf(z01, z11);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
-        }
-        const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
-        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-        const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
-        const float p00 = exp2f(z00 - u0), p01 = exp2f(z01 - u1);
-        const float p10 = exp2f(z10 - u0), p11 = exp2f(z11 - u1);
-        l0 = l0 * al0 + p00 + p10;
-        l1 = l1 * al1 + p01 + p11;
-        m0 = n0;
-        m1 = n1;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
-        }
-        if (A.logits != nullptr) {
-          const int base_tok = info->lp * kP;
-          const size_t hs = (size_t)p.mpp * kP;
-          const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
-          if (v00) A.logits[row0 + h0 * hs + base_tok + g4] = s0 * p.scale;
-          if (v01) A.logits[row0 + h1 * hs + base_tok + g4] = s1 * p.scale;
-          if (v10) A.logits[row0 + h0 * hs + base_tok + g4 + 8] = s2 * p.scale;
-          if (v11) A.logits[row0 + h1 * hs + base_tok + g4 + 8] = s3 * p.scale;
-        }
-        // P (tokens x heads) as bf16 high part + bf16 residual
-        {
-          const __nv_bfloat162 hA = __floats2bfloat162_rn(p00, p01);
-          const __nv_bfloat162 hB = __floats2bfloat162_rn(p10, p11);
-          const float2 fA = __bfloat1622float2(hA), fB = __bfloat1622float2(hB);
-          uint32_t* ph = reinterpret_cast<uint32_t*>(sp);
-          uint32_t* pl = reinterpret_cast<uint32_t*>(sp + 256);
-          ph[g4 * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hA);
-          ph[(g4 + 8) * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hB);
-          pl[g4 * 4 + t4] = pack_bf16(p00 - fA.x, p01 - fA.y);
-          pl[(g4 + 8) * 4 + t4] = pack_bf16(p10 - fB.x, p11 - fB.y);
-        }
-        __syncwarp();
-        uint32_t bh0, bh1, bl0, bl1;
-        ldsm_x2_t(sp_hi + (lane & 15) * 16, bh0, bh1);
-        ldsm_x2_t(sp_lo + (lane & 15) * 16, bl0, bl1);
-        {
-          const int mi = lane >> 3, r = lane & 7;
-          const int tok = (mi >> 1) * 8 + r;
+          for (int off = 4; off < 32; off <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+          }
+          const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+          const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+          const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
+          const float p00 = exp2f(z00 - u0), p01 = exp2f(z01 - u1);
+          const float p10 = exp2f(z10 - u0), p11 = exp2f(z11 - u1);
+          l0 = l0 * al0 + p00 + p10;
+          l1 = l1 * al1 + p01 + p11;
+          m0 = n0;
+          m1 = n1;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(sV + swz(tok, mt * 2 + (mi & 1)), a0, a1, a2, a3);
-            mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+            o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+          }
+          if (A.logits != nullptr) {
+            const int base_tok = info->lp * kP;
+            const size_t hs = (size_t)p.mpp * kP;
+            const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
+            if (v00) A.logits[row0 + h0 * hs + base_tok + g4] = s0 * p.scale;
+            if (v01) A.logits[row0 + h1 * hs + base_tok + g4] = s1 * p.scale;
+            if (v10) A.logits[row0 + h0 * hs + base_tok + g4 + 8] = s2 * p.scale;
+            if (v11) A.logits[row0 + h1 * hs + base_tok + g4 + 8] = s3 * p.scale;
+          }
+          // P (tokens x heads) as bf16 high part + bf16 residual
+          {
+            const __nv_bfloat162 hA = __floats2bfloat162_rn(p00, p01);
+            const __nv_bfloat162 hB = __floats2bfloat162_rn(p10, p11);
+            const float2 fA = __bfloat1622float2(hA), fB = __bfloat1622float2(hB);
+            uint32_t* ph = reinterpret_cast<uint32_t*>(sp);
+            uint32_t* pl = reinterpret_cast<uint32_t*>(sp + 256);
+            ph[g4 * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hA);
+            ph[(g4 + 8) * 4 + t4] = *reinterpret_cast<const uint32_t*>(&hB);
+            pl[g4 * 4 + t4] = pack_bf16(p00 - fA.x, p01 - fA.y);
+            pl[(g4 + 8) * 4 + t4] = pack_bf16(p10 - fB.x, p11 - fB.y);
+          }
+          __syncwarp();
+          uint32_t bh0, bh1, bl0, bl1;
+          ldsm_x2_t(sp_hi + (lane & 15) * 16, bh0, bh1);
+          ldsm_x2_t(sp_lo + (lane & 15) * 16, bl0, bl1);
+          {
+            const int mi = lane >> 3, r = lane & 7;
+            const int tok = (mi >> 1) * 8 + r;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(sV + swz(tok, mt * 2 + (mi & 1)), a0, a1, a2, a3);
+              mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+              mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
           }
         }
+        __syncwarp();   // all lanes done reading the slot (and the P buffer)
+        if (lane == 0) {
+          mbar_arrive(&s_empty[slot]);
+          atomicAdd(&s_misc[16], 1);
+        }
+        ++uses[m];
       }
-      __syncwarp();   // all lanes done reading the slot (and the P buffer)
-      if (lane == 0) mbar_arrive(&s_empty[slot]);
+      const int done = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_misc[16]), 0);
+      if (done >= seg_size) break;
+      if (++spins > (1u << 26)) {   // bounded: a copy never landed
+        if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
+        break;
+      }
     }
     // row sums over the 8 lanes that share t4
 #pragma unroll
@@ -625,6 +676,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         if (tc == 0) A.counters[u] = 0;
       }
     }
+    if (tc == 0) s_misc[16] = 0;   // tiles-done counter of the next segment
     consumer_sync();   // s_w and s_misc are reused by the next segment
   }
 }

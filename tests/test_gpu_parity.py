@@ -242,6 +242,7 @@ def test_lse_merge_standalone():
 
 def test_repeated_calls_reuse_workspace():
     # split-K counters are left at zero: a second call gives the same result
+    # (within rounding: tiles are consumed in the order they land)
     wl = synth.workload("tiny_4k")
     case = synth.make_decode_case(wl, 12)
     ks = synth.k_per_qhead(wl)
@@ -252,4 +253,5 @@ def test_repeated_calls_reuse_workspace():
     idx, cnt, _ = H.gpu_select(prob, dev, summ, ws)
     o1, l1 = H.gpu_decode(prob, dev, idx, cnt, ws)
     o2, l2 = H.gpu_decode(prob, dev, idx, cnt, ws)
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    H.assert_close(o2.cpu().numpy(), o1.cpu().numpy(), "O, second call")
+    H.assert_close(l2.cpu().numpy(), l1.cpu().numpy(), "lse, second call")
