@@ -74,6 +74,8 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
                    const int* __restrict__ sel_idx, const int* __restrict__ sel_cnt, int gran,
                    Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
                    float* __restrict__ lse, int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int flag[];  // [mpp]: page flag, then tile index
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -254,6 +256,8 @@ __device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, int nslots) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // nslots page slots (a multiple of kConsWarps), then small state
@@ -710,9 +714,10 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(build_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.Hk, p.B);
-  build_tiles_kernel<<<grid, kBuildThreads, smem, stream>>>(p, seq_lens, page_table, sel_idx, sel_cnt, gran,
-                                                            static_cast<Tile*>(tiles), ntiles, out, lse, status);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(build_tiles_kernel, grid, dim3(kBuildThreads), smem, stream, p, seq_lens,
+                                   page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, out, lse,
+                                   status);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
@@ -739,8 +744,8 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.lse = lse;
   A.logits = logits;
   A.status = status;
-  decode_kernel<<<grid, kDecThreads, smem, stream>>>(p, A, tmK, tmV, nslots);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace sa

@@ -8,6 +8,8 @@ namespace sa {
 
 __global__ void lse_merge_kernel(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                                  const float* lse_b, float* o, float* lse) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows; r += warps) {
@@ -37,8 +39,9 @@ int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, co
   const int threads = 256;
   long long blocks = ((long long)n_rows * 32 + threads - 1) / threads;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  lse_merge_kernel<<<(int)blocks, threads, 0, stream>>>(n_rows, D, o_a, lse_a, o_b, lse_b, o, lse);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl(lse_merge_kernel, dim3((int)blocks), dim3(threads), 0, stream, n_rows, D, o_a, lse_a, o_b, lse_b, o, lse);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace sa

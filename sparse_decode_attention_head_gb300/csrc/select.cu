@@ -32,6 +32,8 @@ template <int G, int MODE>
 __global__ void __launch_bounds__((kScoreWarps + 1) * 32, 1)
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
              const int* __restrict__ seq_lens, float* __restrict__ scores, int always, int nstages) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kRowElems = (MODE == SA_SUMMARY_MINMAX) ? 2 * kD : kD;
   constexpr int kRowBytes = kRowElems * 2;
   constexpr int kStageBytes = kItemBlocks * kRowBytes + kMaxG * kD * 2;   // summaries + q
@@ -305,6 +307,8 @@ template <int NT, int KPT>
 __global__ void __launch_bounds__(NT)
 topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
             int* __restrict__ sel_idx, int* __restrict__ sel_cnt) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int hist[256];
   __shared__ int s_red[2][NT / 32];
   __shared__ uint32_t s_prefix;
@@ -429,18 +433,19 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   const int nstages = (int)std::min<size_t>(16, (200 * 1024) / stage);
   const size_t smem = stage * nstages;
   const int grid = std::max(1, num_sms);
+  cudaError_t err = cudaSuccess;
 #define SA_SCORE_CASE(GG)                                                                         \
   case GG:                                                                                        \
     if (p.mode == SA_SUMMARY_MINMAX) {                                                            \
       cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MINMAX>,                                   \
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
-      score_kernel<GG, SA_SUMMARY_MINMAX><<<grid, (kScoreWarps + 1) * 32, smem, stream>>>(        \
-          p, qb, sb, seq_lens, scores, always, nstages);                                          \
+      err = launch_pdl(score_kernel<GG, SA_SUMMARY_MINMAX>, dim3(grid), dim3((kScoreWarps + 1) * 32), \
+                       smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
     } else {                                                                                      \
       cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MEAN>,                                     \
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
-      score_kernel<GG, SA_SUMMARY_MEAN><<<grid, (kScoreWarps + 1) * 32, smem, stream>>>(          \
-          p, qb, sb, seq_lens, scores, always, nstages);                                          \
+      err = launch_pdl(score_kernel<GG, SA_SUMMARY_MEAN>, dim3(grid), dim3((kScoreWarps + 1) * 32),   \
+                       smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
     }                                                                                             \
     break;
   switch (p.G) {
@@ -456,7 +461,7 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
       return SA_ERR_UNSUPPORTED;
   }
 #undef SA_SCORE_CASE
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 size_t topk_smem_bytes(const Params&) { return 0; }
@@ -467,15 +472,16 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
   // the largest candidate count any head can have
   int max_n = 0;
   for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  cudaError_t e;
   if (max_n <= 256 * 8)
-    topk_kernel<256, 8><<<grid, 256, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(topk_kernel<256, 8>, grid, dim3(256), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
   else if (max_n <= 1024 * 16)
-    topk_kernel<1024, 16><<<grid, 1024, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(topk_kernel<1024, 16>, grid, dim3(1024), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
   else if (max_n <= 1024 * 64)
-    topk_kernel<1024, 64><<<grid, 1024, 0, stream>>>(p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(topk_kernel<1024, 64>, grid, dim3(1024), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
   else
     return SA_ERR_UNSUPPORTED;
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace sa

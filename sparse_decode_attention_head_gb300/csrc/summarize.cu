@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kSumWarps * 32)
 summarize_kernel(Params p, const __nv_bfloat16* __restrict__ k_pool, const int* __restrict__ page_table,
                  const int* __restrict__ seq_lens, int block_begin, int block_end,
                  __nv_bfloat16* __restrict__ summ, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = min(seq_lens[b], p.mpp * kP);
@@ -122,10 +124,10 @@ int launch_summarize(const Params& p, const void* k_pool, const int* page_table,
   int gx = (span + kSumWarps - 1) / kSumWarps;
   gx = min(gx, 65535);   // the warp loop covers any remainder
   dim3 grid(gx, p.Hk, p.B);
-  summarize_kernel<<<grid, kSumWarps * 32, 0, stream>>>(
-      p, static_cast<const __nv_bfloat16*>(k_pool), page_table, seq_lens, block_begin, block_end,
-      static_cast<__nv_bfloat16*>(summ), status);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(summarize_kernel, grid, dim3(kSumWarps * 32), 0, stream, p,
+                                   static_cast<const __nv_bfloat16*>(k_pool), page_table, seq_lens, block_begin,
+                                   block_end, static_cast<__nv_bfloat16*>(summ), status);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace sa

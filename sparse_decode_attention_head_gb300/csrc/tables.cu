@@ -85,6 +85,8 @@ __device__ void fill_weights(float* w, int base, int n, const TableArgs& A, cons
 
 __global__ void __launch_bounds__(kTabThreads)
 tables_kernel(Params p, TableArgs A) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float s_wv[kChunk + kHalo];       // weights feeding the vertical entries (positions c0-2 ..)
   __shared__ float s_ws[kChunk + kHalo];       // weights feeding the slash entries tested there
   __shared__ unsigned char s_seed[kChunk + kHalo];
@@ -217,8 +219,8 @@ tables_kernel(Params p, TableArgs A) {
 
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream) {
   dim3 grid(p.Hq, p.B);
-  tables_kernel<<<grid, kTabThreads, 0, stream>>>(p, A);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(tables_kernel, grid, dim3(kTabThreads), 0, stream, p, A);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace sa
