@@ -191,6 +191,22 @@ int sa_sparse_decode(const sa_problem* prob, const void* q,
                      int32_t sel_granularity, float* out, float* lse,
                      float* logits_or_null, void* ws, void* stream);
 
+/* One whole decode step for block selection -- a1 (incremental) + a2 + a3 +
+ * a4 + a5 + a6: the same results as
+ *   sa_block_summarize(prob, k_pool, page_table, seq_lens, SA_BLOCKS_TAIL, -1,
+ *                      summaries, ws, stream);
+ *   sa_select_topk(prob, q, summaries, seq_lens, sel_idx, sel_cnt, NULL, ws, stream);
+ *   sa_sparse_decode(prob, q, k_pool, v_pool, page_table, seq_lens, sel_idx,
+ *                    sel_cnt, SA_SEL_BLOCK, out, lse, NULL, ws, stream);
+ * in fewer launches (the top-k, the tile list and the tail-block summary are
+ * one kernel per KV head).  summaries are read for scoring and their tail
+ * block rewritten; sel_idx / sel_cnt receive the selection. */
+int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool,
+                   const void* v_pool, const int32_t* page_table,
+                   const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
+                   int32_t* sel_cnt, float* out, float* lse, void* ws,
+                   void* stream);
+
 /* Step a7 -- score-table update and table-driven candidate selection.
  * Tables: vertical (entry i = absolute position i) and slash (entry d =
  * offset d from the newest token, i.e. position L - 1 - d), fp32

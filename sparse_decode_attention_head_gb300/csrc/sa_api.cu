@@ -48,6 +48,10 @@ struct TableArgs {
   float beta;
 };
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
+int select_build_max_candidates();
+int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
+                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
+                        float* out, float* lse, int* status, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -293,6 +297,47 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
                            at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
                            at<int>(ws, l.header), tmK, tmV, nsm, s);
+}
+
+int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
+                   const int32_t* page_table, const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
+                   int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !summaries || !sel_idx || !sel_cnt || !out || !lse ||
+      !ws)
+    return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SA_ERR_CUDA;
+  CUtensorMap tmK, tmV;
+  if ((rc = make_kv_map(&tmK, k_pool, p)) != SA_OK) return rc;
+  if ((rc = make_kv_map(&tmV, v_pool, p)) != SA_OK) return rc;
+  const Layout l = layout_of(p);
+  cudaStream_t s = as_stream(stream);
+  int* status = at<int>(ws, l.header);
+  float* scores = at<float>(ws, l.scores);
+  // the fused selection holds a head's candidates in registers: up to a bound
+  int max_cand = 0;
+  for (int h = 0; h < p.Hk; ++h) max_cand = std::max(max_cand, (p.mpp * SA_PAGE_SIZE + p.bs[h] - 1) / p.bs[h]);
+  if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
+  if (max_cand <= sa::select_build_max_candidates()) {
+    rc = sa::launch_select_build(p, scores, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt,
+                                 at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, s);
+  } else {
+    if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
+    if ((rc = sa::launch_summarize(p, k_pool, page_table, seq_lens, SA_BLOCKS_TAIL, -1, summaries, status, s)) !=
+        SA_OK)
+      return rc;
+    rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, SA_SEL_BLOCK, at<void>(ws, l.tiles),
+                                at<int>(ws, l.ntiles), out, lse, status, s);
+  }
+  if (rc != SA_OK) return rc;
+  return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
+                           at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);
 }
 
 int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const float* slash_in, float* vert_out,

@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "sa_common.cuh"
+#include "topk.cuh"
 
 namespace sa {
 
@@ -188,239 +189,19 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 
 // ---------------------------------------------------------------- top-k
 
-// One warp selects for one head, so the passes need no block barrier.
-constexpr int kTopkWarpsMax = 4;
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ int warp_incl_scan(int x) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  return x;
-}
-
-// Block-wide exclusive scan of one int per thread; returns the prefix and
-// writes the total to *total.  `tmp` holds >= blockDim.x / 32 ints.
-__device__ __forceinline__ int block_excl_scan(int v, int* tmp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  int x = warp_incl_scan(v);
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? tmp[lane] : 0;
-    w = warp_incl_scan(w);
-    if (lane < nw) tmp[lane] = w;   // inclusive warp totals
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
-  *total = tmp[nw - 1];
-  __syncthreads();
-  return before;
-}
-
-// Warp-collective: the k largest of keys[0, n) by (key desc, index asc),
-// 0 < k < n, written ascending as base_idx + i to out[0, k).  `hist` is 256
-// ints of this warp's shared memory.  MSB-first radix select in 4 passes of 8
-// bits with warp-aggregated histogram updates, then a stable compaction in
-// index order (each lane owns a contiguous index range).
-__device__ void warp_topk(const uint32_t* keys, int n, int k, int* hist, int base_idx, int* out) {
-  const int lane = threadIdx.x & 31;
-  uint32_t prefix = 0, mask = 0;
-  int krem = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) hist[lane * 8 + q] = 0;
-    __syncwarp();
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      const uint32_t u = i < n ? keys[i] : 0u;
-      const bool take = i < n && (u & mask) == prefix;
-      const uint32_t digit = (u >> shift) & 255u;
-      const unsigned act = __ballot_sync(0xffffffffu, take);
-      if (take) {
-        const unsigned peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1) hist[digit] += __popc(peers);   // one writer per digit per round
-      }
-      __syncwarp();
-    }
-    // lane l owns digits 255-8l .. 248-8l (descending)
-    int cnt[8], tot = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) { cnt[q] = hist[255 - 8 * lane - q]; tot += cnt[q]; }
-    const int incl = warp_incl_scan(tot);
-    int above = incl - tot;
-    int found_digit = -1, found_krem = 0;
-    if (above < krem && krem <= incl) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (found_digit < 0 && above < krem && krem <= above + cnt[q]) {
-          found_digit = 255 - 8 * lane - q;
-          found_krem = krem - above;
-        }
-        above += cnt[q];
-      }
-    }
-    const unsigned who = __ballot_sync(0xffffffffu, found_digit >= 0);
-    const int src = __ffs(who) - 1;
-    found_digit = __shfl_sync(0xffffffffu, found_digit, src);
-    found_krem = __shfl_sync(0xffffffffu, found_krem, src);
-    prefix |= (uint32_t)found_digit << shift;
-    mask |= 255u << shift;
-    krem = found_krem;
-    __syncwarp();
-  }
-  const uint32_t T = prefix;   // key of the k-th best
-  const int need_eq = krem;    // keys equal to T that are taken, lowest index first
-  const int per = (n + 31) / 32;
-  const int lo = min(n, lane * per), hi = min(n, lo + per);
-  int eq = 0, gt = 0;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t u = keys[i];
-    eq += u == T;
-    gt += u > T;
-  }
-  const int eq_before = warp_incl_scan(eq) - eq;
-  const int take = gt + max(0, min(eq, need_eq - eq_before));
-  int pos = warp_incl_scan(take) - take;
-  int r = eq_before;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t u = keys[i];
-    bool t = u > T;
-    if (u == T) { t = r < need_eq; ++r; }
-    if (t) out[pos++] = base_idx + i;
-  }
-}
-
-// Block top-k for one (b, head): each thread holds KPT consecutive keys in
-// registers (so the final compaction is already in index order).  The radix
-// passes start below the bits that every key shares (taken from the block's
-// min and max key), so typically 2-3 passes of 8 bits remain.
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT)
 topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
             int* __restrict__ sel_idx, int* __restrict__ sel_cnt) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int hist[256];
-  __shared__ int s_red[2][NT / 32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_krem;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ TopkScratch S;
   const int h = blockIdx.x, b = blockIdx.y;
-  const int kvh = h / p.G;
   const int L = min(seq_lens[b], p.mpp * kP);
   int j0, j1;
-  candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
-  const int n = j1 - j0;
-  const int k = min(p.k[h], n);
-  int* out = sel_idx + ((size_t)b * p.Hq + h) * p.kcap;
-  if (k >= n || k <= 0) {   // keep every candidate (100 % budget, or none) / keep none
-    const int m = k >= n ? n : 0;
-    for (int i = tid; i < m; i += NT) out[i] = j0 + i;
-    if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = m;
-    return;
-  }
-  const float* sc = scores + ((size_t)b * p.Hq + h) * p.slots + j0;
-  uint32_t key[KPT];
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-  for (int q = 0; q < KPT; ++q) {
-    const int i = tid * KPT + q;
-    key[q] = i < n ? order_key(__ldg(sc + i)) : 0u;
-    if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
-  }
-  // block min / max -> the bits all keys share
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) { s_red[0][warp] = (int)kmin; s_red[1][warp] = (int)kmax; }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t a = 0xffffffffu, c = 0u;
-    for (int w = 0; w < NT / 32; ++w) { a = min(a, (uint32_t)s_red[0][w]); c = max(c, (uint32_t)s_red[1][w]); }
-    s_prefix = a;        // temporarily: min
-    s_krem = (int)c;     // temporarily: max
-  }
-  __syncthreads();
-  const uint32_t gmin = s_prefix, gmax = (uint32_t)s_krem;
-  const int common = gmin == gmax ? 32 : __clz(gmin ^ gmax);   // leading bits shared by every key
-  uint32_t mask = common >= 32 ? 0xffffffffu : (common == 0 ? 0u : (0xffffffffu << (32 - common)));
-  uint32_t prefix = gmin & mask;
-  int krem = k;
-  __syncthreads();
-  for (int top = 32 - common; top > 0; top -= 8) {   // bits [top-8, top) are this pass's digit
-    const int shift = max(0, top - 8);
-    const uint32_t dmask = (1u << (top - shift)) - 1u;
-    for (int i = tid; i < 256; i += NT) hist[i] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < KPT; ++q) {
-      const int i = tid * KPT + q;
-      if (i < n && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & dmask], 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits 255-8l .. 248-8l (descending)
-      int cnt[8], tot = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { cnt[q] = hist[255 - 8 * lane - q]; tot += cnt[q]; }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int above = incl - tot;
-      if (above < krem && krem <= incl) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (above < krem && krem <= above + cnt[q]) {
-            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
-            s_krem = krem - above;
-          }
-          above += cnt[q];
-        }
-      }
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    krem = s_krem;
-    mask |= dmask << shift;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;   // key of the k-th best (all 32 bits resolved)
-  const int need_eq = krem;    // keys equal to T that are taken, lowest index first
-  int eq = 0, gt = 0;
-#pragma unroll
-  for (int q = 0; q < KPT; ++q) {
-    const int i = tid * KPT + q;
-    if (i < n) { eq += key[q] == T; gt += key[q] > T; }
-  }
-  int total;
-  const int eq_before = block_excl_scan(eq, &s_red[0][0], &total);
-  const int take = gt + max(0, min(eq, need_eq - eq_before));
-  int pos = block_excl_scan(take, &s_red[1][0], &total);
-  int r = eq_before;
-#pragma unroll
-  for (int q = 0; q < KPT; ++q) {
-    const int i = tid * KPT + q;
-    if (i < n) {
-      bool t = key[q] > T;
-      if (key[q] == T) { t = r < need_eq; ++r; }
-      if (t) out[pos++] = j0 + i;
-    }
-  }
-  if (tid == 0) sel_cnt[(size_t)b * p.Hq + h] = k;
+  candidate_range(L, p.S, p.W, p.bs[h / p.G], j0, j1);
+  group_topk<NT, KPT>(scores + ((size_t)b * p.Hq + h) * p.slots + j0, j1 - j0, p.k[h], j0,
+                      sel_idx + ((size_t)b * p.Hq + h) * p.kcap, sel_cnt + (size_t)b * p.Hq + h, 0, S);
 }
 
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,

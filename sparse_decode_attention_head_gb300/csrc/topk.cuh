@@ -1,0 +1,146 @@
+// Top-k for one head over its candidate blocks: keep the k best by (score
+// descending, block index ascending), reported ascending.  A group of GROUP
+// threads (a whole block, or a slice of one with its own named barrier)
+// holds KPT consecutive keys per thread in registers, finds the k-th key by
+// an MSB-first radix select over order-preserving uint32 keys (starting below
+// the bits every key shares), and compacts in index order.
+#pragma once
+
+#include "sa_common.cuh"
+
+namespace sa {
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void group_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+struct TopkScratch {
+  int hist[256];
+  int red[2][32];
+  uint32_t prefix;
+  int krem;
+};
+
+// Exclusive scan over the group; tmp holds >= GROUP / 32 ints.
+template <int GROUP>
+__device__ __forceinline__ int group_excl_scan(int v, int* tmp, int bar_id) {
+  const int tg = threadIdx.x % GROUP, lane = tg & 31, w = tg >> 5;
+  const int x = warp_incl_scan(v);
+  if (lane == 31) tmp[w] = x;
+  group_sync(bar_id, GROUP);
+  int before = x - v;
+  for (int i = 0; i < w; ++i) before += tmp[i];
+  group_sync(bar_id, GROUP);
+  return before;
+}
+
+// Group-collective.  sc: the head's candidate scores (n of them, block ids
+// base_idx + i); k_req: blocks to keep.  Writes out[0..) and *cnt_out.
+template <int GROUP, int KPT>
+__device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int base_idx, int* __restrict__ out,
+                           int* __restrict__ cnt_out, int bar_id, TopkScratch& S) {
+  const int tg = threadIdx.x % GROUP, lane = tg & 31, w = tg >> 5;
+  const int k = min(k_req, n);
+  if (k >= n || k <= 0) {   // keep every candidate (100 % budget, or none) / keep none
+    const int m = k >= n ? n : 0;
+    for (int i = tg; i < m; i += GROUP) out[i] = base_idx + i;
+    if (tg == 0) *cnt_out = m;
+    return;
+  }
+  uint32_t key[KPT];
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tg * KPT + q;
+    key[q] = i < n ? order_key(sc[i]) : 0u;
+    if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) { S.red[0][w] = (int)kmin; S.red[1][w] = (int)kmax; }
+  group_sync(bar_id, GROUP);
+  uint32_t gmin = 0xffffffffu, gmax = 0u;
+  for (int i = 0; i < GROUP / 32; ++i) { gmin = min(gmin, (uint32_t)S.red[0][i]); gmax = max(gmax, (uint32_t)S.red[1][i]); }
+  group_sync(bar_id, GROUP);
+  const int common = gmin == gmax ? 32 : __clz(gmin ^ gmax);   // leading bits shared by every key
+  uint32_t mask = common >= 32 ? 0xffffffffu : (common == 0 ? 0u : (0xffffffffu << (32 - common)));
+  uint32_t prefix = gmin & mask;
+  int krem = k;
+  for (int top = 32 - common; top > 0; top -= 8) {   // this pass resolves bits [shift, top)
+    const int shift = max(0, top - 8);
+    const uint32_t dmask = (1u << (top - shift)) - 1u;
+    for (int i = tg; i < 256; i += GROUP) S.hist[i] = 0;
+    group_sync(bar_id, GROUP);
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = tg * KPT + q;
+      if (i < n && (key[q] & mask) == prefix) atomicAdd(&S.hist[(key[q] >> shift) & dmask], 1);
+    }
+    group_sync(bar_id, GROUP);
+    if (w == 0) {
+      // lane l owns digits 255-8l .. 248-8l (descending)
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { cnt[q] = S.hist[255 - 8 * lane - q]; tot += cnt[q]; }
+      const int incl = warp_incl_scan(tot);
+      int above = incl - tot;
+      if (above < krem && krem <= incl) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (above < krem && krem <= above + cnt[q]) {
+            S.prefix = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
+            S.krem = krem - above;
+          }
+          above += cnt[q];
+        }
+      }
+    }
+    group_sync(bar_id, GROUP);
+    prefix = S.prefix;
+    krem = S.krem;
+    mask |= dmask << shift;
+    group_sync(bar_id, GROUP);
+  }
+  const uint32_t T = prefix;   // key of the k-th best
+  const int need_eq = krem;    // keys equal to T that are taken, lowest index first
+  int eq = 0, gt = 0;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tg * KPT + q;
+    if (i < n) { eq += key[q] == T; gt += key[q] > T; }
+  }
+  const int eq_before = group_excl_scan<GROUP>(eq, S.red[0], bar_id);
+  const int take = gt + max(0, min(eq, need_eq - eq_before));
+  int pos = group_excl_scan<GROUP>(take, S.red[1], bar_id);
+  int r = eq_before;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int i = tg * KPT + q;
+    if (i < n) {
+      bool t = key[q] > T;
+      if (key[q] == T) { t = r < need_eq; ++r; }
+      if (t) out[pos++] = base_idx + i;
+    }
+  }
+  if (tg == 0) *cnt_out = k;
+}
+
+}  // namespace sa

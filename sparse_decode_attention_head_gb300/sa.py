@@ -76,6 +76,7 @@ def lib():
             "sa_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_lse_merge": (ctypes.c_int, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
+            "sa_decode_step": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                       ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
         }
@@ -264,3 +265,22 @@ def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, s
         _ptr(pv.get("prev_sel_idx")), _ptr(pv.get("prev_sel_cnt")), _ptr(pv.get("prev_logits")),
         _ptr(pv.get("prev_lse")), _ptr(seq_lens), decay, beta, _ptr(cand_idx), _ptr(cand_cnt), _ptr(ws.buf),
         _stream()), "sa_update_score_tables")
+
+
+def decode_step(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse,
+                ws: Workspace):
+    """Whole block-selection decode step: tail-block summary refresh, scores,
+    top-k and the paged sparse decode (sa_decode_step)."""
+    _need(q, torch.bfloat16, "q", (prob.B, prob.Hq, prob.D))
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool", tuple(k_pool.shape))
+    _need(page_table, torch.int32, "page_table", (prob.B, prob.max_pages_per_seq))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    _need(summaries, torch.bfloat16, "summaries", prob.summary_shape())
+    _need(sel_idx, torch.int32, "sel_idx", (prob.B, prob.Hq, prob.kcap))
+    _need(sel_cnt, torch.int32, "sel_cnt", (prob.B, prob.Hq))
+    _need(out, torch.float32, "out", (prob.B, prob.Hq, prob.D))
+    _need(lse, torch.float32, "lse", (prob.B, prob.Hq))
+    _check(lib().sa_decode_step(prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens),
+                                _ptr(summaries), _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf),
+                                _stream()), "sa_decode_step")

@@ -255,3 +255,46 @@ def test_repeated_calls_reuse_workspace():
     o2, l2 = H.gpu_decode(prob, dev, idx, cnt, ws)
     H.assert_close(o2.cpu().numpy(), o1.cpu().numpy(), "O, second call")
     H.assert_close(l2.cpu().numpy(), l1.cpu().numpy(), "lse, second call")
+
+
+@pytest.mark.parametrize("name", ["tiny_4k", "llama_32k", "ragged"])
+def test_decode_step_matches_separate_calls(name):
+    # sa_decode_step = tail summary refresh + select_topk + sparse_decode
+    if name == "ragged":
+        wl = _small(lens=[1500, 1013, 333])
+    else:
+        wl = synth.workload(name)
+    case = synth.make_decode_case(wl, 31)
+    nc = H.to_np_case(case)
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    dev = H.to_dev(case)
+    ws = sa.Workspace(prob)
+    summ = H.gpu_summaries(prob, dev, ws)
+    # poison the tail blocks so the refresh is checked too
+    for b in range(wl.B):
+        L = int(nc.seq_lens[b])
+        for kvh in range(wl.Hk):
+            if L > 0:
+                summ[b, kvh, (L - 1) // wl.block_sizes[kvh]] = 3.0
+    summ_ref = summ.clone()
+    sa.block_summarize(prob, dev["k_pool"], dev["page_table"], dev["seq_lens"], summ_ref, ws,
+                       block_begin=sa.BLOCKS_TAIL)
+    idx_ref, cnt_ref, _ = H.gpu_select(prob, dev, summ_ref, ws, with_scores=False)
+    o_ref, l_ref = H.gpu_decode(prob, dev, idx_ref, cnt_ref, ws)
+    idx = torch.full_like(idx_ref, -5)
+    cnt = torch.full_like(cnt_ref, -5)
+    out = torch.full_like(o_ref, float("nan"))
+    lse = torch.full_like(l_ref, float("nan"))
+    sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx, cnt,
+                   out, lse, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    assert torch.equal(summ.view(torch.int16), summ_ref.view(torch.int16))
+    assert torch.equal(cnt, cnt_ref)
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            n = int(cnt_ref[b, h])
+            assert torch.equal(idx[b, h, :n], idx_ref[b, h, :n])
+    H.assert_close(out.cpu().numpy(), o_ref.cpu().numpy(), "step O")
+    H.assert_close(lse.cpu().numpy(), l_ref.cpu().numpy(), "step lse")
