@@ -17,10 +17,10 @@
 
 namespace sa {
 
-constexpr int kSelThreads = 256;
-constexpr int kSelGroup = 64;                           // threads per head
+constexpr int kSelThreads = 1024;
+constexpr int kSelGroup = 256;                          // threads per head
 constexpr int kSelGroups = kSelThreads / kSelGroup;     // heads selected at once
-constexpr int kSelKpt = 32;                             // keys per thread
+constexpr int kSelKpt = 8;                              // keys per thread
 constexpr int kSelMaxCand = kSelGroup * kSelKpt;        // 2048 candidates per head
 
 __global__ void __launch_bounds__(kSelThreads)
