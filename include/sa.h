@@ -198,8 +198,8 @@ int sa_sparse_decode(const sa_problem* prob, const void* q,
  *   sa_select_topk(prob, q, summaries, seq_lens, sel_idx, sel_cnt, NULL, ws, stream);
  *   sa_sparse_decode(prob, q, k_pool, v_pool, page_table, seq_lens, sel_idx,
  *                    sel_cnt, SA_SEL_BLOCK, out, lse, NULL, ws, stream);
- * in fewer launches (the top-k, the tile list and the tail-block summary are
- * one kernel per KV head).  summaries are read for scoring and their tail
+ * in fewer launches (the tile list and the tail-block summary share one
+ * kernel per KV head).  summaries are read for scoring and their tail
  * block rewritten; sel_idx / sel_cnt receive the selection. */
 int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool,
                    const void* v_pool, const int32_t* page_table,

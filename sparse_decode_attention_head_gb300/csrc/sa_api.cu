@@ -48,10 +48,9 @@ struct TableArgs {
   float beta;
 };
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
-int select_build_max_candidates();
-int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
-                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
-                        float* out, float* lse, int* status, cudaStream_t stream);
+int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
+                      const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
+                      int* status, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -320,21 +319,10 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
   cudaStream_t s = as_stream(stream);
   int* status = at<int>(ws, l.header);
   float* scores = at<float>(ws, l.scores);
-  // the fused selection holds a head's candidates in registers: up to a bound
-  int max_cand = 0;
-  for (int h = 0; h < p.Hk; ++h) max_cand = std::max(max_cand, (p.mpp * SA_PAGE_SIZE + p.bs[h] - 1) / p.bs[h]);
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
-  if (max_cand <= sa::select_build_max_candidates()) {
-    rc = sa::launch_select_build(p, scores, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt,
-                                 at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, s);
-  } else {
-    if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
-    if ((rc = sa::launch_summarize(p, k_pool, page_table, seq_lens, SA_BLOCKS_TAIL, -1, summaries, status, s)) !=
-        SA_OK)
-      return rc;
-    rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, SA_SEL_BLOCK, at<void>(ws, l.tiles),
-                                at<int>(ws, l.ntiles), out, lse, status, s);
-  }
+  if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
+  rc = sa::launch_build_step(p, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt, at<void>(ws, l.tiles),
+                             at<int>(ws, l.ntiles), out, lse, status, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
                            at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);
