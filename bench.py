@@ -280,7 +280,7 @@ def run_ours(args):
 
     # end to end through the public binding: pinned host q in, O + lse out
     e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
-    gpu_launches = 3 * K
+    gpu_launches = 4 * K
 
     res = {
         "metric": METRIC,

@@ -21,7 +21,7 @@
 
 namespace sa {
 
-constexpr int kScoreWarps = 8;                 // consumer warps (+1 producer warp)
+constexpr int kScoreWarps = 16;                // consumer warps (+1 producer warp)
 constexpr int kItemBlocks = 64;                // candidate blocks per work item (8 per consumer warp)
 constexpr int kMaxUnitsScore = 4096;
 
@@ -107,10 +107,19 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   }
 
   // ---------------- consumers
+  // A warp scores 4 blocks at a time (8 lanes per block) for one pair of
+  // heads; the NP pairs of a group of warps cover the G heads of the same 4
+  // blocks, so a warp holds q for two heads only.
+  constexpr int NP = (G + 1) / 2;                      // head pairs
+  constexpr int GROUPS = kScoreWarps / NP;             // 4-block groups per round
+  constexpr int ROUNDS = (kItemBlocks + 4 * GROUPS - 1) / (4 * GROUPS);
+  const int pair = warp % NP, grp = warp / NP;
+  const bool active_warp = grp < GROUPS;
+  const int hA = 2 * pair, hB = 2 * pair + 1;          // this warp's heads (hB may be >= G)
   const int sub = lane >> 3;   // block within the warp's group of 4
   const int part = lane & 7;   // dims [16 part, 16 part + 16)
-  float qf[G][16];
-  uint32_t selw[G][8];
+  float qf[2][16];
+  uint32_t selw[2][8];
   int cur_unit = -1;
   int u = unit_of(it_lo);
   for (int i = 0; i < n_items; ++i) {
@@ -125,62 +134,69 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
     const int st = i % nstages, use = i / nstages;
     if (!mbar_wait_bounded(&s_full[st], use & 1, nullptr)) break;
     const uint8_t* stage = smem + (size_t)st * kStageBytes;
-    if (u != cur_unit) {   // q of the G heads, this lane's 16 dims, fp32 (exact from bf16)
+    if (active_warp && u != cur_unit) {   // q of this warp's heads, this lane's 16 dims, fp32
       cur_unit = u;
       const uint4* qs = reinterpret_cast<const uint4*>(stage + kItemBlocks * kRowBytes);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const uint4 a = qs[g * (kD / 8) + 2 * part], c = qs[g * (kD / 8) + 2 * part + 1];
+      for (int e = 0; e < 2; ++e) {
+        const int g = e == 0 ? hA : hB;
+        const int gg = g < G ? g : 0;
+        const uint4 a = qs[gg * (kD / 8) + 2 * part], c = qs[gg * (kD / 8) + 2 * part + 1];
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-          qf[g][2 * k2] = bf16_lo(w[k2]);
-          qf[g][2 * k2 + 1] = bf16_hi(w[k2]);
-          const bool p0 = qf[g][2 * k2] >= 0.f, p1 = qf[g][2 * k2 + 1] >= 0.f;
+          qf[e][2 * k2] = bf16_lo(w[k2]);
+          qf[e][2 * k2 + 1] = bf16_hi(w[k2]);
+          const bool p0 = qf[e][2 * k2] >= 0.f, p1 = qf[e][2 * k2 + 1] >= 0.f;
           // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
-          selw[g][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
+          selw[e][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
         }
       }
     }
+    if (active_warp) {
 #pragma unroll
-    for (int r = 0; r < kItemBlocks / (4 * kScoreWarps); ++r) {
-      const int cl = (r * kScoreWarps + warp) * 4 + sub;   // block within the item
-      const bool valid = cl < nb;
-      const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
-      uint32_t xmin[8], xmax[8];
-      const uint4 lo0 = base[0], lo1 = base[1];
-      if (MODE == SA_SUMMARY_MINMAX) {
-        const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
-        xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
-        xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
-        xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
-        xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
-      } else {
-        xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
-        xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
+      for (int r = 0; r < ROUNDS; ++r) {
+        const int cl = (r * GROUPS + grp) * 4 + sub;   // block within the item
+        const bool valid = cl < nb;
+        const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
+        uint32_t xmin[8], xmax[8];
+        const uint4 lo0 = base[0], lo1 = base[1];
+        if (MODE == SA_SUMMARY_MINMAX) {
+          const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
+          xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
+          xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
+          xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
+          xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
+        } else {
+          xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
+          xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
-      }
-      float my_score = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-          const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[k2], xmin[k2], selw[g][k2]) : xmax[k2];
-          if (k2 == 0)
-            acc = __fmul_rn(qf[g][0], bf16_lo(w));
-          else
-            acc = __fmaf_rn(qf[g][2 * k2], bf16_lo(w), acc);
-          acc = __fmaf_rn(qf[g][2 * k2 + 1], bf16_hi(w), acc);
+          for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
         }
-        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
-        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
-        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-        acc = __fadd_rn(acc, 0.0f);
-        if (part == g) my_score = acc;
+        float res[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float acc = 0.f;
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2) {
+            const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[k2], xmin[k2], selw[e][k2]) : xmax[k2];
+            if (k2 == 0)
+              acc = __fmul_rn(qf[e][0], bf16_lo(w));
+            else
+              acc = __fmaf_rn(qf[e][2 * k2], bf16_lo(w), acc);
+            acc = __fmaf_rn(qf[e][2 * k2 + 1], bf16_hi(w), acc);
+          }
+          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
+          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
+          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
+          res[e] = __fadd_rn(acc, 0.0f);
+        }
+        // lane part 0 writes head hA, part 1 writes head hB
+        if (valid && part < 2) {
+          const int g = part == 0 ? hA : hB;
+          if (g < G) scores[((size_t)b * p.Hq + kvh * G + g) * p.slots + j0 + first + cl] = part == 0 ? res[0] : res[1];
+        }
       }
-      if (valid && part < G) scores[((size_t)b * p.Hq + kvh * G + part) * p.slots + j0 + first + cl] = my_score;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_empty[st]);
