@@ -84,8 +84,31 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 
   if (warp == kScoreWarps) {   // ---------------- producer
     if (lane == 0) {
+      // L2 prefetch runs a full ring of stages ahead of the loads, so a
+      // stage refill finds its summaries in L2
+      auto item_src = [&](int i, int& bytes) -> const void* {
+        const long long it = it_lo + i;
+        const int uu = unit_of(it);
+        const int b = uu / p.Hk, kvh = uu % p.Hk;
+        const int L = min(seq_lens[b], p.mpp * kP);
+        int j0, j1;
+        candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+        const int first = (int)(it - s_items[uu]) * kItemBlocks;
+        bytes = min(kItemBlocks, (j1 - j0) - first) * kRowBytes;
+        return summ + ((((size_t)b * p.Hk + kvh) * p.slots) + j0 + first) * kRowElems;
+      };
+      for (int i = nstages; i < min(n_items, 2 * nstages); ++i) {
+        int bytes;
+        const void* src = item_src(i, bytes);
+        bulk_prefetch_l2(src, bytes);
+      }
       int u = unit_of(it_lo);
       for (int i = 0; i < n_items; ++i) {
+        if (i + 2 * nstages < n_items) {
+          int bytes;
+          const void* src = item_src(i + 2 * nstages, bytes);
+          bulk_prefetch_l2(src, bytes);
+        }
         const long long it = it_lo + i;
         while (it >= s_items[u + 1]) ++u;
         const int b = u / p.Hk, kvh = u % p.Hk;
