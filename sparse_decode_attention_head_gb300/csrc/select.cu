@@ -176,16 +176,32 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         }
       }
     }
+    // copy this warp's blocks out of the stage, release it, then compute:
+    // the producer can refill the stage while the arithmetic runs
+    uint4 dlo[ROUNDS][2], dhi[ROUNDS][2];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int cl = (r * GROUPS + grp) * 4 + sub;
+      const bool valid = active_warp && cl < nb;
+      const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
+      dlo[r][0] = base[0];
+      dlo[r][1] = base[1];
+      if (MODE == SA_SUMMARY_MINMAX) {
+        dhi[r][0] = base[kD / 8];
+        dhi[r][1] = base[kD / 8 + 1];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[st]);
     if (active_warp) {
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
         const int cl = (r * GROUPS + grp) * 4 + sub;   // block within the item
         const bool valid = cl < nb;
-        const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
         uint32_t xmin[8], xmax[8];
-        const uint4 lo0 = base[0], lo1 = base[1];
+        const uint4 lo0 = dlo[r][0], lo1 = dlo[r][1];
         if (MODE == SA_SUMMARY_MINMAX) {
-          const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
+          const uint4 hi0 = dhi[r][0], hi1 = dhi[r][1];
           xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
           xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
           xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
@@ -221,8 +237,6 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_empty[st]);
   }
 }
 
