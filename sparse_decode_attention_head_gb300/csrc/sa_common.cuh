@@ -156,10 +156,21 @@ __device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, u
       : "memory");
 }
 
-// 1-D bulk prefetch of global memory into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
-               : "memory");
+// d = a * b + c in fp32 where a, b are the low (or high) bf16 halves of two
+// packed words.  Widening bf16 to fp32 is exact, so this is
+// fmaf(float(a), float(b), c) with its single rounding; with c = -0 it is
+// the plain product, signed zeros included.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
 }
 
 // 2-D tiled TMA load of one box into shared memory, completion on `bar`.

@@ -84,31 +84,8 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 
   if (warp == kScoreWarps) {   // ---------------- producer
     if (lane == 0) {
-      // L2 prefetch runs a full ring of stages ahead of the loads, so a
-      // stage refill finds its summaries in L2
-      auto item_src = [&](int i, int& bytes) -> const void* {
-        const long long it = it_lo + i;
-        const int uu = unit_of(it);
-        const int b = uu / p.Hk, kvh = uu % p.Hk;
-        const int L = min(seq_lens[b], p.mpp * kP);
-        int j0, j1;
-        candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
-        const int first = (int)(it - s_items[uu]) * kItemBlocks;
-        bytes = min(kItemBlocks, (j1 - j0) - first) * kRowBytes;
-        return summ + ((((size_t)b * p.Hk + kvh) * p.slots) + j0 + first) * kRowElems;
-      };
-      for (int i = nstages; i < min(n_items, 2 * nstages); ++i) {
-        int bytes;
-        const void* src = item_src(i, bytes);
-        bulk_prefetch_l2(src, bytes);
-      }
       int u = unit_of(it_lo);
       for (int i = 0; i < n_items; ++i) {
-        if (i + 2 * nstages < n_items) {
-          int bytes;
-          const void* src = item_src(i + 2 * nstages, bytes);
-          bulk_prefetch_l2(src, bytes);
-        }
         const long long it = it_lo + i;
         while (it >= s_items[u + 1]) ++u;
         const int b = u / p.Hk, kvh = u % p.Hk;
@@ -141,7 +118,7 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   const int hA = 2 * pair, hB = 2 * pair + 1;          // this warp's heads (hB may be >= G)
   const int sub = lane >> 3;   // block within the warp's group of 4
   const int part = lane & 7;   // dims [16 part, 16 part + 16)
-  float qf[2][16];
+  uint32_t qw[2][8];
   uint32_t selw[2][8];
   int cur_unit = -1;
   int u = unit_of(it_lo);
@@ -168,40 +145,23 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-          qf[e][2 * k2] = bf16_lo(w[k2]);
-          qf[e][2 * k2 + 1] = bf16_hi(w[k2]);
-          const bool p0 = qf[e][2 * k2] >= 0.f, p1 = qf[e][2 * k2 + 1] >= 0.f;
+          qw[e][k2] = w[k2];
+          const bool p0 = bf16_lo(w[k2]) >= 0.f, p1 = bf16_hi(w[k2]) >= 0.f;
           // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
           selw[e][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
         }
       }
     }
-    // copy this warp's blocks out of the stage, release it, then compute:
-    // the producer can refill the stage while the arithmetic runs
-    uint4 dlo[ROUNDS][2], dhi[ROUNDS][2];
-#pragma unroll
-    for (int r = 0; r < ROUNDS; ++r) {
-      const int cl = (r * GROUPS + grp) * 4 + sub;
-      const bool valid = active_warp && cl < nb;
-      const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
-      dlo[r][0] = base[0];
-      dlo[r][1] = base[1];
-      if (MODE == SA_SUMMARY_MINMAX) {
-        dhi[r][0] = base[kD / 8];
-        dhi[r][1] = base[kD / 8 + 1];
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_empty[st]);
     if (active_warp) {
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
         const int cl = (r * GROUPS + grp) * 4 + sub;   // block within the item
         const bool valid = cl < nb;
+        const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
         uint32_t xmin[8], xmax[8];
-        const uint4 lo0 = dlo[r][0], lo1 = dlo[r][1];
+        const uint4 lo0 = base[0], lo1 = base[1];
         if (MODE == SA_SUMMARY_MINMAX) {
-          const uint4 hi0 = dhi[r][0], hi1 = dhi[r][1];
+          const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
           xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
           xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
           xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
@@ -219,11 +179,9 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 #pragma unroll
           for (int k2 = 0; k2 < 8; ++k2) {
             const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[k2], xmin[k2], selw[e][k2]) : xmax[k2];
-            if (k2 == 0)
-              acc = __fmul_rn(qf[e][0], bf16_lo(w));
-            else
-              acc = __fmaf_rn(qf[e][2 * k2], bf16_lo(w), acc);
-            acc = __fmaf_rn(qf[e][2 * k2 + 1], bf16_hi(w), acc);
+            // fma with c = -0 is the plain product, zero signs included
+            acc = fma_bf16_lo(qw[e][k2], w, k2 == 0 ? -0.0f : acc);
+            acc = fma_bf16_hi(qw[e][k2], w, acc);
           }
           acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
           acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
@@ -237,6 +195,8 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[st]);
   }
 }
 
