@@ -21,14 +21,43 @@
 
 namespace sa {
 
-constexpr int kScoreWarps = 16;                // consumer warps (+1 producer warp)
-constexpr int kItemBlocks = 64;                // candidate blocks per work item (8 per consumer warp)
+constexpr int kScoreWarps = 15;                // consumer warps (+1 producer warp: 4 warps per scheduler)
 constexpr int kMaxUnitsScore = 4096;
 
 // Work items are (unit = (b, kv head), run of kItemBlocks candidate blocks).
 // Each CTA takes a contiguous range of items; a producer thread streams each
 // item's summaries (contiguous) and the group's q into a ring of shared-memory
-// stages with 1-D bulk copies; consumer warps score the staged blocks.
+// stages with 1-D bulk copies, and leaves a descriptor of the item (where its
+// scores go, how many blocks it holds) beside the stage; consumer warps score
+// the staged blocks.
+struct ItemDesc {
+  long long sbase;   // scores index of (b, first head of the group, first block of the item)
+  int nb;            // blocks in the item
+  int unit;          // b * Hk + kvh
+};
+
+// Work split for a group of G query heads.  A consumer warp scores 4 blocks
+// at a time (8 lanes per block) for a set of up to 4 heads (q is held packed,
+// 8 registers per head, plus 8 selector words per head for min/max); the head
+// sets of a group of warps cover the G heads of the same 4 blocks, so each
+// staged summary byte is read from shared memory once per head set.  An item
+// is as many blocks as the consumer warps take in kRounds passes.
+template <int G>
+struct ScoreShape {
+  static constexpr int kPerWarp = G < 4 ? G : 4;
+  static constexpr int kSets = (G + kPerWarp - 1) / kPerWarp;
+  static constexpr int kGroups = kScoreWarps / kSets;   // 4-block groups per pass
+  static constexpr int kRounds = kSets == 1 ? 1 : 2;
+  static constexpr int kItemBlocks = 4 * kGroups * kRounds;
+};
+
+constexpr int item_blocks(int G) {
+  return G == 1 ? ScoreShape<1>::kItemBlocks : G == 2 ? ScoreShape<2>::kItemBlocks
+       : G == 3 ? ScoreShape<3>::kItemBlocks : G == 4 ? ScoreShape<4>::kItemBlocks
+       : G == 5 ? ScoreShape<5>::kItemBlocks : G == 6 ? ScoreShape<6>::kItemBlocks
+       : G == 7 ? ScoreShape<7>::kItemBlocks : ScoreShape<8>::kItemBlocks;
+}
+
 template <int G, int MODE>
 __global__ void __launch_bounds__((kScoreWarps + 1) * 32, 1)
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
@@ -37,9 +66,11 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   pdl_trigger();
   constexpr int kRowElems = (MODE == SA_SUMMARY_MINMAX) ? 2 * kD : kD;
   constexpr int kRowBytes = kRowElems * 2;
+  constexpr int kItemBlocks = ScoreShape<G>::kItemBlocks;
   constexpr int kStageBytes = kItemBlocks * kRowBytes + kMaxG * kD * 2;   // summaries + q
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t s_full[16], s_empty[16];
+  __shared__ ItemDesc s_desc[16];
   __shared__ int s_items[kMaxUnitsScore + 1];   // prefix of items over units
 
   const int U = p.B * p.Hk;
@@ -63,9 +94,15 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    s_items[0] = 0;
-    for (int u = 0; u < U; ++u) s_items[u + 1] += s_items[u];
+  if (warp == 0) {   // inclusive scan of the item counts, 32 units at a time
+    int carry = 0;
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      const int x = warp_incl_scan(u < U ? s_items[u + 1] : 0);
+      if (u < U) s_items[u + 1] = x + carry;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s_items[0] = 0;
   }
   __syncthreads();
   const long long total = s_items[U];
@@ -73,19 +110,16 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   const int n_items = (int)(it_hi - it_lo);
   if (n_items <= 0) return;
 
-  auto unit_of = [&](long long it) {
-    int lo = 0, hi = U;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_items[mid] <= it) lo = mid; else hi = mid;
-    }
-    return lo;
-  };
-
   if (warp == kScoreWarps) {   // ---------------- producer
     if (lane == 0) {
-      int u = unit_of(it_lo);
+      int lo = 0, hi = U;   // unit holding the first item
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_items[mid] <= it_lo) lo = mid; else hi = mid;
+      }
+      int u = lo;
       for (int i = 0; i < n_items; ++i) {
+        // describe the item before waiting for its stage
         const long long it = it_lo + i;
         while (it >= s_items[u + 1]) ++u;
         const int b = u / p.Hk, kvh = u % p.Hk;
@@ -96,8 +130,9 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         const int nb = min(kItemBlocks, (j1 - j0) - first);
         const int st = i % nstages, use = i / nstages;
         if (use > 0 && !mbar_wait_bounded(&s_empty[st], (use - 1) & 1, nullptr)) break;
+        s_desc[st] = ItemDesc{((long long)b * p.Hq + kvh * G) * p.slots + j0 + first, nb, u};
         uint8_t* dst = smem + (size_t)st * kStageBytes;
-        mbar_arrive_expect_tx(&s_full[st], nb * kRowBytes + G * kD * 2);
+        mbar_arrive_expect_tx(&s_full[st], nb * kRowBytes + G * kD * 2);   // release: orders s_desc
         bulk_load_1d(dst, summ + ((((size_t)b * p.Hk + kvh) * p.slots) + j0 + first) * kRowElems, nb * kRowBytes,
                      &s_full[st]);
         bulk_load_1d(dst + kItemBlocks * kRowBytes, q + ((size_t)b * p.Hq + kvh * G) * kD, G * kD * 2, &s_full[st]);
@@ -107,74 +142,65 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   }
 
   // ---------------- consumers
-  // A warp scores 4 blocks at a time (8 lanes per block) for one pair of
-  // heads; the NP pairs of a group of warps cover the G heads of the same 4
-  // blocks, so a warp holds q for two heads only.
-  constexpr int NP = (G + 1) / 2;                      // head pairs
-  constexpr int GROUPS = kScoreWarps / NP;             // 4-block groups per round
-  constexpr int ROUNDS = (kItemBlocks + 4 * GROUPS - 1) / (4 * GROUPS);
-  const int pair = warp % NP, grp = warp / NP;
+  constexpr int HPW = ScoreShape<G>::kPerWarp;
+  constexpr int NS = ScoreShape<G>::kSets;
+  constexpr int GROUPS = ScoreShape<G>::kGroups;
+  constexpr int ROUNDS = ScoreShape<G>::kRounds;
+  const int hset = warp % NS, grp = warp / NS;
   const bool active_warp = grp < GROUPS;
-  const int hA = 2 * pair, hB = 2 * pair + 1;          // this warp's heads (hB may be >= G)
   const int sub = lane >> 3;   // block within the warp's group of 4
   const int part = lane & 7;   // dims [16 part, 16 part + 16)
-  uint32_t qw[2][8];
-  uint32_t selw[2][8];
+  uint32_t qw[HPW][8];         // q of the warp's heads, this lane's 16 dims, packed bf16
+  uint32_t selw[HPW][8];       // byte selectors: kmax where q >= 0, else kmin
   int cur_unit = -1;
-  int u = unit_of(it_lo);
   for (int i = 0; i < n_items; ++i) {
-    const long long it = it_lo + i;
-    while (it >= s_items[u + 1]) ++u;
-    const int b = u / p.Hk, kvh = u % p.Hk;
-    const int L = min(seq_lens[b], p.mpp * kP);
-    int j0, j1;
-    candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
-    const int first = (int)(it - s_items[u]) * kItemBlocks;
-    const int nb = min(kItemBlocks, (j1 - j0) - first);
     const int st = i % nstages, use = i / nstages;
     if (!mbar_wait_bounded(&s_full[st], use & 1, nullptr)) break;
+    const ItemDesc dsc = s_desc[st];
     const uint8_t* stage = smem + (size_t)st * kStageBytes;
-    if (active_warp && u != cur_unit) {   // q of this warp's heads, this lane's 16 dims, fp32
-      cur_unit = u;
-      const uint4* qs = reinterpret_cast<const uint4*>(stage + kItemBlocks * kRowBytes);
+    if (active_warp) {
+      if (dsc.unit != cur_unit) {
+        cur_unit = dsc.unit;
+        const uint4* qs = reinterpret_cast<const uint4*>(stage + kItemBlocks * kRowBytes);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int g = e == 0 ? hA : hB;
-        const int gg = g < G ? g : 0;
-        const uint4 a = qs[gg * (kD / 8) + 2 * part], c = qs[gg * (kD / 8) + 2 * part + 1];
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        for (int e = 0; e < HPW; ++e) {
+          const int g = hset * HPW + e;
+          const int gg = g < G ? g : 0;
+          const uint4 a = qs[gg * (kD / 8) + 2 * part], c = qs[gg * (kD / 8) + 2 * part + 1];
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-          qw[e][k2] = w[k2];
-          const bool p0 = bf16_lo(w[k2]) >= 0.f, p1 = bf16_hi(w[k2]) >= 0.f;
-          // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
-          selw[e][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
+          for (int k2 = 0; k2 < 8; ++k2) {
+            qw[e][k2] = w[k2];
+            const bool p0 = bf16_lo(w[k2]) >= 0.f, p1 = bf16_hi(w[k2]) >= 0.f;
+            // result bytes 0,1 from kmax (0,1) or kmin (4,5); bytes 2,3 from kmax (2,3) or kmin (6,7)
+            selw[e][k2] = (p0 ? 0x10u : 0x54u) | (p1 ? 0x3200u : 0x7600u);
+          }
         }
       }
-    }
-    if (active_warp) {
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
         const int cl = (r * GROUPS + grp) * 4 + sub;   // block within the item
-        const bool valid = cl < nb;
+        const bool valid = cl < dsc.nb;
         const uint4* base = reinterpret_cast<const uint4*>(stage + (size_t)(valid ? cl : 0) * kRowBytes) + 2 * part;
         uint32_t xmin[8], xmax[8];
-        const uint4 lo0 = base[0], lo1 = base[1];
-        if (MODE == SA_SUMMARY_MINMAX) {
-          const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
-          xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
-          xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
-          xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
-          xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
-        } else {
-          xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
-          xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
+        {
+          const uint4 lo0 = base[0], lo1 = base[1];
+          if (MODE == SA_SUMMARY_MINMAX) {
+            const uint4 hi0 = base[kD / 8], hi1 = base[kD / 8 + 1];
+            xmin[0] = lo0.x; xmin[1] = lo0.y; xmin[2] = lo0.z; xmin[3] = lo0.w;
+            xmin[4] = lo1.x; xmin[5] = lo1.y; xmin[6] = lo1.z; xmin[7] = lo1.w;
+            xmax[0] = hi0.x; xmax[1] = hi0.y; xmax[2] = hi0.z; xmax[3] = hi0.w;
+            xmax[4] = hi1.x; xmax[5] = hi1.y; xmax[6] = hi1.z; xmax[7] = hi1.w;
+          } else {
+            xmax[0] = lo0.x; xmax[1] = lo0.y; xmax[2] = lo0.z; xmax[3] = lo0.w;
+            xmax[4] = lo1.x; xmax[5] = lo1.y; xmax[6] = lo1.z; xmax[7] = lo1.w;
 #pragma unroll
-          for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
+            for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
+          }
         }
-        float res[2];
+        float res[HPW];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int e = 0; e < HPW; ++e) {
           float acc = 0.f;
 #pragma unroll
           for (int k2 = 0; k2 < 8; ++k2) {
@@ -188,11 +214,13 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
           acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
           res[e] = __fadd_rn(acc, 0.0f);
         }
-        // lane part 0 writes head hA, part 1 writes head hB
-        if (valid && part < 2) {
-          const int g = part == 0 ? hA : hB;
-          if (g < G) scores[((size_t)b * p.Hq + kvh * G + g) * p.slots + j0 + first + cl] = part == 0 ? res[0] : res[1];
-        }
+        // lane part e writes head hset * HPW + e
+        float v = res[0];
+#pragma unroll
+        for (int e = 1; e < HPW; ++e)
+          if (part == e) v = res[e];
+        const int g = hset * HPW + part;
+        if (valid && part < HPW && g < G) scores[dsc.sbase + (long long)g * p.slots + cl] = v;
       }
     }
     __syncwarp();
@@ -223,7 +251,7 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* sb = static_cast<const __nv_bfloat16*>(summ);
   const int row_bytes = (p.mode == SA_SUMMARY_MINMAX ? 2 : 1) * kD * 2;
-  const size_t stage = (size_t)kItemBlocks * row_bytes + kMaxG * kD * 2;
+  const size_t stage = (size_t)item_blocks(p.G) * row_bytes + kMaxG * kD * 2;
   const int nstages = (int)std::min<size_t>(16, (200 * 1024) / stage);
   const size_t smem = stage * nstages;
   const int grid = std::max(1, num_sms);
