@@ -40,7 +40,10 @@ namespace sa {
 
 constexpr int kConsWarps = 4;                      // consumer warps
 constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
-constexpr int kMaxCtas = 1024;                     // grid cap (partial slots are sized for it)
+constexpr int kMaxCtas = 512;                      // grid cap (partial slots are sized for it)
+constexpr int kChunksPerCta = 8;                   // chunk size: about this many chunks per CTA ...
+constexpr int kMinChunk = 8;                       // ... but at least this many tiles
+constexpr int kChunkRing = 32;                     // published chunks not yet finished (> slots)
 constexpr int kMaxSlotsPerWarp = 4;                // slots <= 16
 constexpr int kPart = kD + 2;                      // floats per head in a partial: O[kD], max, sum
 constexpr int kSlab = kP * kD * 2;           // 4096 bytes: one page of one KV head
@@ -55,9 +58,10 @@ __global__ void __launch_bounds__(kBuildThreads)
 build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                    const int* __restrict__ sel_idx, const int* __restrict__ sel_cnt, int gran,
                    Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
-                   float* __restrict__ lse, int* status) {
+                   float* __restrict__ lse, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
   extern __shared__ int flag[];  // [mpp]: page flag, then tile index
   __shared__ int scan_tmp[32];
   build_unit_tiles(p, blockIdx.y, blockIdx.x, seq_lens, page_table, sel_idx, sel_cnt, gran, tiles, ntiles, out, lse,
@@ -71,8 +75,9 @@ struct DecodeArgs {
   const int* page_table;
   const Tile* tiles;
   const int* ntiles;
-  float* partials;   // [kMaxCtas][2][G][kPart]
-  int* counters;     // [U]
+  float* partials;   // [chunks][partial_stride(G)]: per chunk O[G][kD], max[G], sum[G]
+  int* chunk_prefix; // [U + 1]: chunks before unit u (written by CTA 0 for the merge kernel)
+  int* ticket;       // chunk ticket counter (zeroed by the tile builder)
   float* out;
   float* lse;
   float* logits;     // may be null
@@ -80,7 +85,7 @@ struct DecodeArgs {
 };
 
 struct __align__(16) SlotInfo {
-  int unit, lp, phys, pad;
+  int unit, lp, phys, seq;   // seq: the CTA's chunk ordinal the tile belongs to
   uint32_t mask[4];
 };
 
@@ -90,16 +95,16 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)((chunk >> 3) * kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsWarps * 32) : "memory");
-}
 
-// CTA whose slice [c T / n, (c+1) T / n) holds global tile x.
-__device__ __forceinline__ int cta_of(long long x, long long T, int n) {
-  return (int)(((x + 1) * n + T - 1) / T) - 1;
-}
-
-__device__ __forceinline__ long long slice_lo(int c, long long T, int n) { return (long long)c * T / n; }
+// Chunk c of the unit-major chunk list: unit, position in the unit, tiles.
+struct ChunkInfo {
+  int unit;   // -1: no more chunks
+  int kin;    // chunk index within the unit
+  int nch;    // chunks of the unit
+  int t0;     // first tile (within the unit's list)
+  int nt;     // tiles in the chunk
+  int pad[3];
+};
 
 // Unit u with prefix[u] <= x < prefix[u + 1] (prefix non-decreasing, x < prefix[U]).
 __device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
@@ -111,6 +116,21 @@ __device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
   return lo;
 }
 
+// Floats per chunk partial: O[G][kD], then max[G] and sum[G], padded to 16 bytes.
+__host__ __device__ __forceinline__ int partial_stride(int G) { return (G * (kD + 2) + 3) & ~3; }
+
+__device__ __forceinline__ int ld_volatile(const int* x) { return *reinterpret_cast<const volatile int*>(x); }
+// CTA-scope acquire load / release store (ordering the chunk ring between
+// the producer warp and the consumer warps)
+__device__ __forceinline__ int ld_acquire_cta(const int* x) {
+  int v;
+  asm volatile("ld.acquire.cta.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta(int* x, int v) {
+  asm volatile("st.release.cta.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
+}
+
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, int nslots) {
@@ -118,19 +138,24 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int G = p.G;
+  const int U = p.B * p.Hk;
   // nslots page slots (a multiple of kConsWarps), then small state
   uint8_t* s_tiles = smem;                                                   // nslots * kTileBytes
   uint8_t* s_p = s_tiles + (size_t)nslots * kTileBytes;                      // kConsWarps * 512
   float* s_w = reinterpret_cast<float*>(s_p + kConsWarps * 512);             // kConsWarps * G * kPart
-  SlotInfo* s_info = reinterpret_cast<SlotInfo*>(s_w + kConsWarps * p.G * kPart);   // nslots
-  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_info + nslots);           // nslots
+  SlotInfo* s_info = reinterpret_cast<SlotInfo*>(s_w + kConsWarps * G * kPart);   // nslots
+  ChunkInfo* s_chunk = reinterpret_cast<ChunkInfo*>(s_info + nslots);       // kChunkRing
+  int* s_assign = reinterpret_cast<int*>(s_chunk + kChunkRing);             // kChunkRing * kConsWarps
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_assign + kChunkRing * kConsWarps);   // nslots
   uint64_t* s_empty = s_full + nslots;                                       // nslots
   int* s_misc = reinterpret_cast<int*>(s_empty + nslots);                    // 32 ints
-  int* s_prefix = s_misc + 32;                                               // U + 1
+  int* s_prefix = s_misc + 32;                                               // U + 1: tiles before unit u
+  int* s_cprefix = s_prefix + U + 1;                                         // U + 1: chunks before unit u
+  // s_misc: [17] chunks published, [18] chunks combined, [19] chunks fully
+  // issued, [20] consumer warps parked on the current chunk
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.G;
-  const int U = p.B * p.Hk;
 
   if (tid == 0) {
     for (int i = 0; i < nslots; ++i) {
@@ -138,12 +163,16 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       mbar_init(&s_empty[i], 1);
     }
     fence_mbar_init();
-    s_misc[16] = 0;
+    s_misc[17] = 0;
+    s_misc[18] = 0;
+    s_misc[19] = 0;
+    s_misc[20] = 0;
   }
-  // prefix over the units' tile counts (block-wide scan)
+  // prefix over the units' tile counts (block-wide scan); the chunk size
+  // follows from the total so that every CTA derives the same chunk list
+  const int per = (U + blockDim.x - 1) / blockDim.x;
+  const int a = min(U, tid * per), e = min(U, a + per);
   {
-    const int per = (U + blockDim.x - 1) / blockDim.x;
-    const int a = min(U, tid * per), e = min(U, a + per);
     int cnt = 0;
     for (int i = a; i < e; ++i) cnt += A.ntiles[i];
     int x = cnt;
@@ -163,116 +192,231 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     if (tid == blockDim.x - 1) s_prefix[U] = before;
   }
   __syncthreads();
-  const long long T = s_prefix[U];
-  // slice over n_eff = min(grid, T) CTAs so that every slice is non-empty: the
-  // split-unit merge counts one arrival per CTA index between two slices
-  const int nC = (int)min((long long)gridDim.x, T), c = blockIdx.x;
-  if (c >= nC) return;
-  const long long lo = slice_lo(c, T, nC), hi = slice_lo(c + 1, T, nC);
-  if (lo >= hi) return;
-  const int n_local = (int)(hi - lo);
+  const int T = s_prefix[U];
+  const int C = max(kMinChunk, (T + kChunksPerCta * (int)gridDim.x - 1) / (kChunksPerCta * (int)gridDim.x));
+  {
+    int cnt = 0;
+    for (int i = a; i < e; ++i) cnt += (s_prefix[i + 1] - s_prefix[i] + C - 1) / C;
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_misc[warp] = x;
+    __syncthreads();
+    int before = x - cnt;
+    for (int w2 = 0; w2 < warp; ++w2) before += s_misc[w2];
+    for (int i = a; i < e; ++i) {
+      s_cprefix[i] = before;
+      before += (s_prefix[i + 1] - s_prefix[i] + C - 1) / C;
+    }
+    if (tid == blockDim.x - 1) s_cprefix[U] = before;
+  }
+  __syncthreads();
+  const int NCH = s_cprefix[U];
+  const int PS = partial_stride(G);
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= U; i += blockDim.x) A.chunk_prefix[i] = s_cprefix[i];
 
   // ------------------------------------------------------------ producer warp
-  // Lane j (< nslots) owns slot j and issues that slot's uses in order.  The
-  // slice's tiles are handed out in order to whichever slots are free, so a
-  // tile that lands late holds back only its own slot.  Descriptors come in
-  // batches of 32 (one per lane, the next batch loaded ahead) and are passed
-  // to the issuing lane by shuffle.
+  // Takes chunks from the global ticket counter (one taken ahead) and
+  // publishes each in the chunk ring before issuing its tiles.  Lane j
+  // (< nslots) owns slot j and issues that slot's uses in order; a chunk's
+  // tiles go to whichever slots are free, so a tile that lands late holds
+  // back only its own slot.  Descriptors (one per lane, up to 32 at a time)
+  // reach the issuing lane by shuffle.  Once a chunk is fully issued, the
+  // number of its tiles each consumer warp received (slot j belongs to warp
+  // j mod kConsWarps) is published, so every warp knows when its share is done.
   if (warp == kConsWarps) {
     const bool owner = lane < nslots;
-    int use = 0, next = 0, dbase = 0;
-    int4 dA0, dB0;
-    uint4 dA1, dB1;
-    auto load_desc = [&](int base_, int4& w0, uint4& w1) {
-      const int i = base_ + lane;
-      if (i < n_local) {
-        const long long t = lo + i;
-        const int uu = unit_of(s_prefix, U, t);
-        const Tile* tp = A.tiles + (size_t)uu * p.mpp + (t - s_prefix[uu]);
-        w0 = __ldg(reinterpret_cast<const int4*>(tp));
-        w1 = __ldg(reinterpret_cast<const uint4*>(&tp->mask[0]));
-        w0.z = uu;   // the unit rides in a pad field
-      } else {
-        w0 = make_int4(0, -1, 0, 0);
-        w1 = make_uint4(0, 0, 0, 0);
+    int use = 0;
+    auto chunk_info = [&](int t) {
+      ChunkInfo c;
+      c.unit = -1;
+      c.kin = c.nch = c.t0 = c.nt = 0;
+      c.pad[0] = c.pad[1] = c.pad[2] = 0;
+      if (t < NCH) {
+        const int u = unit_of(s_cprefix, U, t);
+        c.unit = u;
+        c.kin = t - s_cprefix[u];
+        c.nch = s_cprefix[u + 1] - s_cprefix[u];
+        c.t0 = c.kin * C;
+        c.nt = min(C, s_prefix[u + 1] - s_prefix[u] - c.t0);
+      }
+      return c;
+    };
+    // descriptors of tiles [b0, b0 + 32) of chunk c, one per lane
+    auto load_desc = [&](const ChunkInfo& c, int b0, int4& w0, uint4& w1) {
+      w0 = make_int4(0, -1, 0, 0);
+      w1 = make_uint4(0, 0, 0, 0);
+      if (c.unit >= 0 && b0 + lane < c.nt) {
+        const Tile* t = A.tiles + (size_t)c.unit * p.mpp + c.t0 + b0 + lane;
+        w0 = __ldg(reinterpret_cast<const int4*>(t));
+        w1 = __ldg(reinterpret_cast<const uint4*>(&t->mask[0]));
       }
     };
-    load_desc(0, dA0, dA1);
-    load_desc(32, dB0, dB1);
+    int tk = 0;
+    if (lane == 0) tk = atomicAdd(A.ticket, 1);
+    ChunkInfo ci = chunk_info(__shfl_sync(0xffffffffu, tk, 0));
+    int4 dA0;
+    uint4 dA1;
+    load_desc(ci, 0, dA0, dA1);
     uint32_t spins = 0;
-    while (next < n_local) {
-      const bool free_slot = owner && (use == 0 || mbar_test_wait(&s_empty[lane], (use - 1) & 1));
-      const unsigned fm = __ballot_sync(0xffffffffu, free_slot);
-      const int n_issue = min(__popc(fm), min(32 - (next - dbase), n_local - next));
-      const int rank = __popc(fm & ((1u << lane) - 1u));
-      const bool mine = free_slot && rank < n_issue;
-      const int src = next - dbase + (mine ? rank : 0);
-      int4 w0;
-      uint4 w1;
-      w0.x = __shfl_sync(0xffffffffu, dA0.x, src);
-      w0.y = __shfl_sync(0xffffffffu, dA0.y, src);
-      w0.z = __shfl_sync(0xffffffffu, dA0.z, src);
-      w1.x = __shfl_sync(0xffffffffu, dA1.x, src);
-      w1.y = __shfl_sync(0xffffffffu, dA1.y, src);
-      w1.z = __shfl_sync(0xffffffffu, dA1.z, src);
-      w1.w = __shfl_sync(0xffffffffu, dA1.w, src);
-      if (mine) {
-        const int slot = lane, u = w0.z;
-        const int phys = (w0.y >= 0 && w0.y < p.num_pages) ? w0.y : -1;
-        SlotInfo info;
-        info.unit = u;
-        info.lp = w0.x;
-        info.phys = phys;
-        info.pad = 0;
-        info.mask[0] = w1.x; info.mask[1] = w1.y; info.mask[2] = w1.z; info.mask[3] = w1.w;
-        s_info[slot] = info;
-        if (phys >= 0) {
-          uint8_t* dst = s_tiles + (size_t)slot * kTileBytes;
-          const int row = (phys * p.Hk + (u % p.Hk)) * kP;
-          mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
-          tma_load_2d(dst, &tmK, 0, row, &s_full[slot]);
-          tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_full[slot]);
-          tma_load_2d(dst + kSlab, &tmV, 0, row, &s_full[slot]);
-          tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_full[slot]);
-        } else {
-          mbar_arrive(&s_full[slot]);
+    bool stop = false;
+    for (int k = 0; !stop; ++k) {
+      // ring space: the consumers have finished chunk k - kChunkRing
+      while (k >= kChunkRing && ld_acquire_cta(&s_misc[18]) <= k - kChunkRing) {
+        if (++spins > (1u << 28)) {
+          if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
+          ci.unit = -1;
+          break;
         }
-        ++use;
       }
-      next += n_issue;
-      if (next - dbase >= 32) {   // move to the next batch and load the one after it
-        dA0 = dB0;
-        dA1 = dB1;
-        dbase += 32;
-        load_desc(dbase + 32, dB0, dB1);
+      if (lane == 0) {
+        s_chunk[k % kChunkRing] = ci;
+        st_release_cta(&s_misc[17], k + 1);
       }
-      if (n_issue == 0 && ++spins > (1u << 28)) {   // bounded: consumers stopped releasing slots
-        set_status(A.status, SA_ERR_TIMEOUT);
+      __syncwarp();
+      if (ci.unit < 0) break;
+      // the next chunk's ticket is taken now and read (its descriptors
+      // fetched) the first time this chunk waits for a free slot
+      int nxt = 0;
+      if (lane == 0) nxt = atomicAdd(A.ticket, 1);
+      bool have_next = false;
+      int asg[kConsWarps];
+#pragma unroll
+      for (int w = 0; w < kConsWarps; ++w) asg[w] = 0;
+      ChunkInfo cn;
+      int4 dB0;
+      uint4 dB1;
+      auto fetch_next = [&]() {
+        cn = chunk_info(__shfl_sync(0xffffffffu, nxt, 0));
+        load_desc(cn, 0, dB0, dB1);
+        have_next = true;
+      };
+      for (int b0 = 0; b0 < ci.nt && !stop; b0 += 32) {
+        const int nb = min(32, ci.nt - b0);
+        int4 dw0 = dA0;
+        uint4 dw1 = dA1;
+        if (b0 > 0) load_desc(ci, b0, dw0, dw1);
+        int next = 0;
+        while (next < nb) {
+          const bool free_slot = owner && (use == 0 || mbar_test_wait(&s_empty[lane], (use - 1) & 1));
+          const unsigned fm = __ballot_sync(0xffffffffu, free_slot);
+          const int n_issue = min(__popc(fm), nb - next);
+          const int rank = __popc(fm & ((1u << lane) - 1u));
+          const bool mine = free_slot && rank < n_issue;
+          const int src = next + (mine ? rank : 0);
+          const int lp = __shfl_sync(0xffffffffu, dw0.x, src);
+          const int ph = __shfl_sync(0xffffffffu, dw0.y, src);
+          uint4 w1;
+          w1.x = __shfl_sync(0xffffffffu, dw1.x, src);
+          w1.y = __shfl_sync(0xffffffffu, dw1.y, src);
+          w1.z = __shfl_sync(0xffffffffu, dw1.z, src);
+          w1.w = __shfl_sync(0xffffffffu, dw1.w, src);
+          if (mine) {
+            const int slot = lane;
+            const int phys = (ph >= 0 && ph < p.num_pages) ? ph : -1;
+            SlotInfo info;
+            info.unit = ci.unit;
+            info.lp = lp;
+            info.phys = phys;
+            info.seq = k;
+            info.mask[0] = w1.x; info.mask[1] = w1.y; info.mask[2] = w1.z; info.mask[3] = w1.w;
+            s_info[slot] = info;
+            if (phys >= 0) {
+              uint8_t* dst = s_tiles + (size_t)slot * kTileBytes;
+              const int row = (phys * p.Hk + (ci.unit % p.Hk)) * kP;
+              mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
+              tma_load_2d(dst, &tmK, 0, row, &s_full[slot]);
+              tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_full[slot]);
+              tma_load_2d(dst + kSlab, &tmV, 0, row, &s_full[slot]);
+              tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_full[slot]);
+            } else {
+              mbar_arrive(&s_full[slot]);
+            }
+            ++use;
+          }
+          next += n_issue;
+          {
+            const unsigned im = __ballot_sync(0xffffffffu, mine);
+#pragma unroll
+            for (int w = 0; w < kConsWarps; ++w) asg[w] += __popc(im & (0x11111111u << w));
+          }
+          if (n_issue == 0) {
+            if (!have_next) fetch_next();
+            if (++spins > (1u << 28)) {   // bounded: consumers stopped releasing slots
+              if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
+              stop = true;
+              break;
+            }
+          }
+        }
+      }
+      if (stop) {   // tell the consumers there is nothing more
+        if (lane == 0) {
+          ChunkInfo end;
+          end.unit = -1;
+          s_chunk[(k + 1) % kChunkRing] = end;
+          st_release_cta(&s_misc[17], k + 2);
+        }
         break;
       }
+      if (lane == 0) {
+#pragma unroll
+        for (int w = 0; w < kConsWarps; ++w) s_assign[(k % kChunkRing) * kConsWarps + w] = asg[w];
+        st_release_cta(&s_misc[19], k + 1);
+      }
+      if (!have_next) fetch_next();
+      ci = cn;
+      dA0 = dB0;
+      dA1 = dB1;
     }
     return;
   }
 
   // ------------------------------------------------------------ consumer warps
+  // Each warp runs through the chunks on its own: it takes the landed slots
+  // of the current chunk, and once it has processed its share it parks its
+  // state (O, max, sum per head) in s_w and moves on.  The last warp to park
+  // a chunk combines the parked states and writes the chunk's partial (or the
+  // output, for a unit held in one chunk); parking the next chunk waits for
+  // that combine, so the warps are never more than one chunk apart.
   const float scale_log2 = p.scale * 1.4426950408889634f;
   const int g4 = lane >> 2, t4 = lane & 3;
   uint8_t* sp = s_p + warp * 512;
   const uint32_t sp_hi = smem_u32(sp), sp_lo = sp_hi + 256;
-  const int tc = tid;   // consumer thread index == head-dim index in the merges (kConsWarps * 32 == kD)
   int uses[kMaxSlotsPerWarp];   // completed uses of each of this warp's slots
 #pragma unroll
   for (int m = 0; m < kMaxSlotsPerWarp; ++m) uses[m] = 0;
+  int q_unit = -1;
+  uint32_t qb[8][2];
 
-  for (int u = unit_of(s_prefix, U, lo); u < U && s_prefix[u] < hi; ++u) {
-    const long long ub = s_prefix[u], ue = s_prefix[u + 1];
-    const long long sb = max(lo, ub), se = min(hi, ue);
-    if (sb >= se) continue;
+  // bounded wait (lane 0 polls, the warp follows) until *x > v; false on timeout
+  auto wait_gt = [&](const int* x, int v) {
+    int ok = 1;
+    if (lane == 0) {
+      uint32_t spins = 0;
+      while (ld_acquire_cta(x) <= v) {
+        if (++spins > (1u << 26)) { ok = 0; break; }
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    if (!ok && lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
+    return ok != 0;
+  };
+
+  for (int k = 0;; ++k) {
+    if (!wait_gt(&s_misc[17], k)) break;   // chunk k published
+    const ChunkInfo ci = s_chunk[k % kChunkRing];
+    if (ci.unit < 0) break;
+    const int u = ci.unit;
     const int b = u / p.Hk, kvh = u % p.Hk;
 
-    // Q fragments (B operand: k = dim, n = head), heads >= G are zero
-    uint32_t qb[8][2];
-    {
+    if (u != q_unit) {   // Q fragments (B operand: k = dim, n = head), heads >= G are zero
+      q_unit = u;
       const bool hv = g4 < G;
       const uint32_t* qrow =
           reinterpret_cast<const uint32_t*>(A.q + ((size_t)b * p.Hq + kvh * G + (hv ? g4 : 0)) * kD);
@@ -287,12 +431,12 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    const int seg_size = (int)(se - sb);
     // poll this warp's slots (warp, warp + kConsWarps, ...) and take whichever
-    // has landed; a slot holding a later unit's tile is left for its segment
+    // has landed; a slot holding a later chunk's tile is left for that chunk
     bool held[kMaxSlotsPerWarp];
 #pragma unroll
     for (int m = 0; m < kMaxSlotsPerWarp; ++m) held[m] = false;
+    int done = 0;
     uint32_t spins = 0;
     while (true) {
 #pragma unroll
@@ -302,7 +446,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         const bool ready = __shfl_sync(0xffffffffu, (int)mbar_test_wait(&s_full[slot], uses[m] & 1), 0) != 0;
         if (!ready) continue;
         const SlotInfo* info = s_info + slot;
-        if (info->unit != u) {
+        if (info->seq != k) {
           held[m] = true;
           continue;
         }
@@ -391,14 +535,15 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
           }
         }
         __syncwarp();   // all lanes done reading the slot (and the P buffer)
-        if (lane == 0) {
-          mbar_arrive(&s_empty[slot]);
-          atomicAdd(&s_misc[16], 1);
-        }
+        if (lane == 0) mbar_arrive(&s_empty[slot]);
         ++uses[m];
+        ++done;
       }
-      const int done = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_misc[16]), 0);
-      if (done >= seg_size) break;
+      // this warp's share of the chunk is known once the chunk is fully issued
+      int fin = 0;
+      if (lane == 0 && ld_acquire_cta(&s_misc[19]) > k)
+        fin = done >= s_assign[(k % kChunkRing) * kConsWarps + warp];
+      if (__shfl_sync(0xffffffffu, fin, 0)) break;
       if (++spins > (1u << 26)) {   // bounded: a copy never landed
         if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
         break;
@@ -410,7 +555,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    // ---- merge the consumer warps' states: s_w[warp][head][kPart]
+    // ---- park: s_w[warp][head][kPart], once the previous chunk is combined
+    if (!wait_gt(&s_misc[18], k - 1)) break;
     {
       float* ww = s_w + warp * G * kPart;
       const bool w0ok = 2 * t4 < G, w1ok = 2 * t4 + 1 < G;
@@ -431,121 +577,122 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         if (w1ok) { ww[(2 * t4 + 1) * kPart + kD] = m1; ww[(2 * t4 + 1) * kPart + kD + 1] = l1; }
       }
     }
-    consumer_sync();
-    const bool whole = ub >= lo && ue <= hi;
-    const int pslot = ub <= lo ? 0 : 1;   // this CTA's first segment, or its last
-    float* part = A.partials + ((size_t)c * 2 + pslot) * G * kPart;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&s_misc[20], 1) == kConsWarps - 1;
+      __threadfence_block();
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+    // ---- the last warp combines the kConsWarps states: lane owns dims [4 lane, 4 lane + 4)
+    if (lane == 0) s_misc[20] = 0;
+    const bool whole = ci.nch == 1;
+    float* part = A.partials + (size_t)(s_cprefix[u] + ci.kin) * PS;
     for (int g = 0; g < G; ++g) {
       float M = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kConsWarps; ++ww) M = fmaxf(M, s_w[(ww * G + g) * kPart + kD]);
-      float acc = 0.f, l = 0.f;
+      for (int w = 0; w < kConsWarps; ++w) M = fmaxf(M, s_w[(w * G + g) * kPart + kD]);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int ww = 0; ww < kConsWarps; ++ww) {
-          const float mw = s_w[(ww * G + g) * kPart + kD];
+        for (int w = 0; w < kConsWarps; ++w) {
+          const float* sw = s_w + (w * G + g) * kPart;
+          const float mw = sw[kD];
           const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-          acc += f * s_w[(ww * G + g) * kPart + tc];
-          l += f * s_w[(ww * G + g) * kPart + kD + 1];
+          const float2 x0 = *reinterpret_cast<const float2*>(sw + 4 * lane);
+          const float2 x1 = *reinterpret_cast<const float2*>(sw + 4 * lane + 2);
+          acc.x += f * x0.x;
+          acc.y += f * x0.y;
+          acc.z += f * x1.x;
+          acc.w += f * x1.y;
+          l += f * sw[kD + 1];
         }
       }
       if (whole) {
         const size_t row = (size_t)b * p.Hq + kvh * G + g;
-        A.out[row * kD + tc] = l > 0.f ? acc / l : 0.f;
-        if (tc == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        *reinterpret_cast<float4*>(A.out + row * kD + 4 * lane) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (lane == 0) A.lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
       } else {
-        part[g * kPart + tc] = acc;
-        if (tc == 0) {
-          part[g * kPart + kD] = M;
-          part[g * kPart + kD + 1] = l;
+        *reinterpret_cast<float4*>(part + g * kD + 4 * lane) = acc;
+        if (lane == 0) {
+          part[G * kD + g] = M;
+          part[G * kD + G + g] = l;
         }
       }
     }
-    if (!whole) {
-      __threadfence();
-      consumer_sync();
-      const int c_first = cta_of(ub, T, nC), c_last = cta_of(ue - 1, T, nC);
-      if (tc == 0) {
-        const int prev = atomicAdd(&A.counters[u], 1);
-        s_misc[0] = (prev == c_last - c_first);
-      }
-      consumer_sync();
-      if (s_misc[0]) {
-        __threadfence();
-        // Merge the CTAs' partials in CTA order.  The (max, sum) of every
-        // (partial, head) is staged in shared memory (s_w is free here) so
-        // the loads overlap instead of forming a dependent chain.
-        const int np = c_last - c_first + 1;
-        const int chunk = 256 / G;            // partials per staging round (2 x 256 floats fit s_w)
-        float* sm_a = s_w;                    // [chunk][G]: max, then weight
-        float* sm_b = s_w + 256;              // [chunk][G]: sum
-        float* sm_M = reinterpret_cast<float*>(s_misc + 8);   // [G]: running max
-        if (tc < G) sm_M[tc] = -INFINITY;
-        consumer_sync();
-        for (int base = 0; base < np; base += chunk) {
-          const int nb = min(np - base, chunk);
-          for (int idx = tc; idx < nb * G; idx += kConsWarps * 32) {
-            const int cc = c_first + base + idx / G, g = idx % G;
-            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
-            sm_a[idx] = __ldcg(A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart + kD);
-          }
-          consumer_sync();
-          if (tc < G) {
-            float M = sm_M[tc];
-            for (int j = 0; j < nb; ++j) M = fmaxf(M, sm_a[j * G + tc]);
-            sm_M[tc] = M;
-          }
-          consumer_sync();
-        }
-        float accs[kMaxG], ls[kMaxG];
-#pragma unroll
-        for (int g = 0; g < kMaxG; ++g) { accs[g] = 0.f; ls[g] = 0.f; }
-        for (int base = 0; base < np; base += chunk) {
-          const int nb = min(np - base, chunk);
-          for (int idx = tc; idx < nb * G; idx += kConsWarps * 32) {
-            const int cc = c_first + base + idx / G, g = idx % G;
-            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
-            const float* pc = A.partials + (((size_t)cc * 2 + ps) * G + g) * kPart;
-            const float mc = __ldcg(pc + kD), M = sm_M[g];
-            sm_a[idx] = (mc == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mc - M);
-            sm_b[idx] = __ldcg(pc + kD + 1);
-          }
-          consumer_sync();
-#pragma unroll 4
-          for (int j = 0; j < nb; ++j) {
-            const int cc = c_first + base + j;
-            const int ps = ub <= slice_lo(cc, T, nC) ? 0 : 1;
-            const float* pc = A.partials + ((size_t)cc * 2 + ps) * G * kPart;
-#pragma unroll
-            for (int g = 0; g < kMaxG; ++g) {
-              if (g < G) {
-                const float f = sm_a[j * G + g];
-                accs[g] += f * __ldcg(pc + g * kPart + tc);
-                ls[g] += f * sm_b[j * G + g];
-              }
-            }
-          }
-          consumer_sync();
-        }
-#pragma unroll
-        for (int g = 0; g < kMaxG; ++g) {
-          if (g < G) {
-            const size_t row = (size_t)b * p.Hq + kvh * G + g;
-            A.out[row * kD + tc] = ls[g] > 0.f ? accs[g] / ls[g] : 0.f;
-            if (tc == 0) A.lse[row] = ls[g] > 0.f ? (sm_M[g] + log2f(ls[g])) * 0.6931471805599453f : -INFINITY;
-          }
-        }
-        if (tc == 0) A.counters[u] = 0;
-      }
-    }
-    if (tc == 0) s_misc[16] = 0;   // tiles-done counter of the next segment
-    consumer_sync();   // s_w and s_misc are reused by the next segment
+    __syncwarp();
+    if (lane == 0) st_release_cta(&s_misc[18], k + 1);   // chunk k combined: s_w and the ring entry are free
   }
+}
+
+// ------------------------------------------------------------------ merge
+
+// One CTA per (query head g of the group, unit u): the exact log-sum-exp
+// merge of the unit's chunk partials in chunk order; thread d owns dim d.
+// Units held in one chunk (or none) were finished by the decode kernel.
+// One pass with a running maximum: the (max, sum, O) loads of kMergeIn
+// chunks are issued together, then the running sums are rescaled once to
+// the batch's maximum and the batch is added.
+constexpr int kMergeThreads = kD;
+constexpr int kMergeIn = 16;
+
+__global__ void __launch_bounds__(kMergeThreads)
+merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __restrict__ chunk_prefix,
+                    float* __restrict__ out, float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
+  const int g = blockIdx.x, u = blockIdx.y;
+  const int c0 = chunk_prefix[u], nch = chunk_prefix[u + 1] - c0;
+  if (nch <= 1) return;
+  const int G = p.G, PS = partial_stride(G);
+  const int tid = threadIdx.x;
+  const float* P = partials + (size_t)c0 * PS;
+  float M = -INFINITY, acc = 0.f, l = 0.f;
+  for (int j0 = 0; j0 < nch; j0 += kMergeIn) {
+    float vm[kMergeIn], vl[kMergeIn], vo[kMergeIn];
+#pragma unroll
+    for (int t = 0; t < kMergeIn; ++t) {
+      if (j0 + t < nch) {
+        const float* pc = P + (size_t)(j0 + t) * PS;
+        vm[t] = __ldcg(pc + G * kD + g);
+        vl[t] = __ldcg(pc + G * kD + G + g);
+        vo[t] = __ldcg(pc + g * kD + tid);
+      } else {
+        vm[t] = -INFINITY;
+        vl[t] = 0.f;
+        vo[t] = 0.f;
+      }
+    }
+    float Mb = M;
+#pragma unroll
+    for (int t = 0; t < kMergeIn; ++t) Mb = fmaxf(Mb, vm[t]);
+    if (Mb == -INFINITY) continue;
+    const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);
+    acc *= r;
+    l *= r;
+#pragma unroll
+    for (int t = 0; t < kMergeIn; ++t) {
+      const float w = vm[t] == -INFINITY ? 0.f : exp2f(vm[t] - Mb);
+      acc += w * vo[t];
+      l += w * vl[t];
+    }
+    M = Mb;
+  }
+  const int b = u / p.Hk, kvh = u % p.Hk;
+  const size_t row = (size_t)b * p.Hq + kvh * G + g;
+  out[row * kD + tid] = l > 0.f ? acc / l : 0.f;
+  if (tid == 0) lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
 }
 
 size_t decode_smem_bytes_n(int U, int G, int nslots) {
   return 1024 + (size_t)nslots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * G * kPart * 4 +
-         nslots * sizeof(SlotInfo) + 2 * nslots * 8 + 32 * 4 + (size_t)(U + 1) * 4;
+         nslots * sizeof(SlotInfo) + kChunkRing * sizeof(ChunkInfo) + kChunkRing * kConsWarps * 4 +
+         2 * nslots * 8 + 32 * 4 +
+         2 * (size_t)(U + 1) * 4;
 }
 
 // Slot count: the largest multiple of kConsWarps (<= 16) that still lets two
@@ -560,13 +707,17 @@ int decode_slots(int U, int G) {
 
 size_t decode_smem_bytes(int U) { return decode_smem_bytes_n(U, kMaxG, kConsWarps); }
 
-size_t decode_partials_bytes(const Params& p) { return (size_t)kMaxCtas * 2 * p.G * kPart * sizeof(float); }
+// Chunks never exceed kChunksPerCta * grid + U (the chunk size grows with the
+// total beyond kMinChunk tiles per chunk), and the grid never exceeds kMaxCtas.
+size_t decode_partials_bytes(const Params& p) {
+  return ((size_t)kChunksPerCta * kMaxCtas + (size_t)p.B * p.Hk) * partial_stride(p.G) * sizeof(float);
+}
 
 size_t tiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * p.mpp * sizeof(Tile); }
 
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       cudaStream_t stream) {
+                       int* ticket, cudaStream_t stream) {
   const size_t smem = (size_t)p.mpp * sizeof(int);
   if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
@@ -574,7 +725,7 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
   dim3 grid(p.Hk, p.B);
   const cudaError_t e = launch_pdl(build_tiles_kernel, grid, dim3(kBuildThreads), smem, stream, p, seq_lens,
                                    page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, out, lse,
-                                   status);
+                                   status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -597,12 +748,16 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.tiles = static_cast<const Tile*>(tiles);
   A.ntiles = ntiles;
   A.partials = partials;
-  A.counters = counters;
+  A.chunk_prefix = counters;
+  A.ticket = counters + U + 1;
   A.out = out;
   A.lse = lse;
   A.logits = logits;
   A.status = status;
-  const cudaError_t e = launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
+  cudaError_t e = launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
+  if (e != cudaSuccess) return SA_ERR_CUDA;
+  e = launch_pdl(merge_chunks_kernel, dim3(p.G, U), dim3(kMergeThreads), 0, stream, p,
+                 static_cast<const float*>(partials), static_cast<const int*>(counters), out, lse);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -2,7 +2,8 @@
 // allocate device memory.
 //
 // sa_sparse_decode needs a caller-allocated workspace for its scratch (the
-// per-KV-head tile lists, the split-K partials and their arrival counters).
+// per-KV-head tile lists, the split-K chunk partials, the chunk prefix and
+// the chunk ticket).
 // Some callers cannot provide one: code that runs inside a host framework
 // which owns every device allocation through its own pool and forbids any
 // other cudaMalloc, or a latency-critical path where cudaMalloc's implicit
@@ -14,8 +15,8 @@
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
 // that device current) and caches it.  Every call shares the array and it
-// keeps the last call's contents: the arrival counters and the status word
-// are cleared at the start of each call, and two calls that overlap on the
+// keeps the last call's contents: the status word is cleared at the start of
+// each call (the tile builder zeroes the chunk ticket), and two calls that overlap on the
 // GPU (different streams, or different host threads) race on it.
 #include <cuda.h>
 
@@ -26,7 +27,7 @@
 namespace sa {
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       cudaStream_t stream);
+                       int* ticket, cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
@@ -62,8 +63,8 @@ NoAllocLayout layout_of(const sa::Params& p) {
   size_t off = 0;
   l.status = off;
   off = up256(off + sizeof(int));
-  l.counters = off;
-  off = up256(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
+  off = up256(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
   l.ntiles = off;
   off = up256(off + (size_t)p.B * p.Hk * sizeof(int));
   l.tiles = off;
@@ -121,11 +122,11 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   char* b = static_cast<char*>(base);
   int* status = status_or_null ? status_or_null : reinterpret_cast<int*>(b + l.status);
   int* counters = reinterpret_cast<int*>(b + l.counters);
-  // what must start at zero: the status word and the split-K arrival counters
+  // what must start at zero: the status word (the tile builder zeroes the
+  // chunk ticket; the decode writes the chunk prefix before the merge reads it)
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
-  if (cudaMemsetAsync(counters, 0, (size_t)p.B * p.Hk * sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
-                              reinterpret_cast<int*>(b + l.ntiles), out, lse, status, s);
+                              reinterpret_cast<int*>(b + l.ntiles), out, lse, status, counters + p.B * p.Hk + 1, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
                            reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,

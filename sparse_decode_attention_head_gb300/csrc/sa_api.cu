@@ -21,7 +21,7 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
 size_t topk_smem_bytes(const Params& p);
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       cudaStream_t stream);
+                       int* ticket, cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
@@ -50,7 +50,7 @@ struct TableArgs {
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
-                      int* status, cudaStream_t stream);
+                      int* status, int* ticket, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -122,8 +122,8 @@ Layout layout_of(const Params& p) {
   off = align_up(off + sa::tiles_bytes(p));
   l.ntiles = off;
   off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
-  l.counters = off;
-  off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
+  off = align_up(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
   l.partials = off;
   off = align_up(off + sa::decode_partials_bytes(p));
   l.total = off;
@@ -291,7 +291,8 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   const Layout l = layout_of(p);
   cudaStream_t s = as_stream(stream);
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
-                              at<int>(ws, l.ntiles), out, lse, at<int>(ws, l.header), s);
+                              at<int>(ws, l.ntiles), out, lse, at<int>(ws, l.header),
+                              at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
                            at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
@@ -322,7 +323,7 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
   if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
   rc = sa::launch_build_step(p, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt, at<void>(ws, l.tiles),
-                             at<int>(ws, l.ntiles), out, lse, status, s);
+                             at<int>(ws, l.ntiles), out, lse, status, at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
                            at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);

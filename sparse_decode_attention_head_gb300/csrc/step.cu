@@ -25,9 +25,10 @@ __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                   const __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ summ, const int* sel_idx,
                   const int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
-                  float* __restrict__ lse, int* status) {
+                  float* __restrict__ lse, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
   extern __shared__ int flag[];   // [mpp] for the tile builder
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -40,7 +41,7 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
-                      int* status, cudaStream_t stream) {
+                      int* status, int* ticket, cudaStream_t stream) {
   const size_t smem = (size_t)p.mpp * sizeof(int);
   if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
@@ -48,7 +49,7 @@ int launch_build_step(const Params& p, const int* seq_lens, const int* page_tabl
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
                                    seq_lens, page_table, static_cast<const __nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(summ), sel_idx, sel_cnt, static_cast<Tile*>(tiles),
-                                   ntiles, out, lse, status);
+                                   ntiles, out, lse, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
