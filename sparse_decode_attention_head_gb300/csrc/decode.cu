@@ -62,10 +62,12 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
-  extern __shared__ int flag[];  // [mpp]: page flag, then tile index
+  extern __shared__ int smem_b[];   // build_smem_bytes(mpp): window flags, then window masks
   __shared__ int scan_tmp[32];
-  build_unit_tiles(p, blockIdx.y, blockIdx.x, seq_lens, page_table, sel_idx, sel_cnt, gran, tiles, ntiles, out, lse,
-                   status, flag, scan_tmp);
+  const int win = min(p.mpp, kWinPages);
+  build_unit_tiles<kBuildThreads>(p, blockIdx.y, blockIdx.x, seq_lens, page_table, sel_idx, sel_cnt, gran, tiles,
+                                  ntiles, out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win),
+                                  scan_tmp);
 }
 
 // ------------------------------------------------------------------ decode
@@ -256,9 +258,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
         w1 = __ldg(reinterpret_cast<const uint4*>(&t->mask[0]));
       }
     };
-    int tk = 0;
-    if (lane == 0) tk = atomicAdd(A.ticket, 1);
-    ChunkInfo ci = chunk_info(__shfl_sync(0xffffffffu, tk, 0));
+    // CTA c starts on chunk c; later chunks come from the ticket counter
+    ChunkInfo ci = chunk_info(blockIdx.x);
     int4 dA0;
     uint4 dA1;
     load_desc(ci, 0, dA0, dA1);
@@ -282,7 +283,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       // the next chunk's ticket is taken now and read (its descriptors
       // fetched) the first time this chunk waits for a free slot
       int nxt = 0;
-      if (lane == 0) nxt = atomicAdd(A.ticket, 1);
+      if (lane == 0) nxt = (int)gridDim.x + atomicAdd(A.ticket, 1);
       bool have_next = false;
       int asg[kConsWarps];
 #pragma unroll
@@ -718,8 +719,7 @@ size_t tiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * p.mpp * sizeof
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
                        int* ticket, cudaStream_t stream) {
-  const size_t smem = (size_t)p.mpp * sizeof(int);
-  if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  const size_t smem = build_smem_bytes(p.mpp);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(build_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.Hk, p.B);

@@ -16,10 +16,11 @@
 
 namespace sa {
 
-// Tile list of one (sequence, KV head) plus the incremental summary of its
-// block holding token L - 1 (warp 0 does the summary first, the rest of the
-// block starts on the tile list meanwhile).
+// Tile list of one (sequence, KV head) by warps 0..30, and the incremental
+// summary of its block holding token L - 1 by warp 31, which takes no part
+// in the builder's barriers.
 constexpr int kStepBuildThreads = 1024;
+constexpr int kStepTileThreads = kStepBuildThreads - 32;
 
 __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
@@ -29,21 +30,24 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
-  extern __shared__ int flag[];   // [mpp] for the tile builder
+  extern __shared__ int smem_b[];   // build_smem_bytes(mpp): window flags, then window masks
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int L = min(seq_lens[b], p.mpp * kP);
-  if (threadIdx.x < 32 && L > 0)
-    summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
-  build_unit_tiles(p, b, kvh, seq_lens, page_table, sel_idx, sel_cnt, SA_SEL_BLOCK, tiles, ntiles, out, lse, status,
-                   flag, scan_tmp);
+  if (threadIdx.x >= kStepTileThreads) {
+    const int L = min(seq_lens[b], p.mpp * kP);
+    if (L > 0)
+      summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
+    return;
+  }
+  const int win = min(p.mpp, kWinPages);
+  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx, sel_cnt, SA_SEL_BLOCK, tiles, ntiles,
+                                     out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
 }
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
                       int* status, int* ticket, cudaStream_t stream) {
-  const size_t smem = (size_t)p.mpp * sizeof(int);
-  if (smem > 200 * 1024) return SA_ERR_UNSUPPORTED;
+  const size_t smem = build_smem_bytes(p.mpp);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(build_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,

@@ -27,137 +27,160 @@ __device__ __forceinline__ void item_range(int gran, int x, int Bs, int Lc, int 
   }
 }
 
-// Block-collective: build the tile list of unit (b, kvh).  `flag` is
-// shared memory of max_pages_per_seq ints, `scan_tmp` 32 ints.
+// Pages per builder window: the builder keeps a flag and 16 token masks per
+// page of the current window in shared memory (20 bytes a page).
+constexpr int kWinPages = 4096;
+
+__host__ __device__ inline size_t build_smem_bytes(int mpp) {
+  const int w = mpp < kWinPages ? mpp : kWinPages;
+  return (size_t)w * (sizeof(int) + 4 * sizeof(uint32_t));
+}
+
+// Collective over threads [0, NT) (named barrier 1): build the tile list of
+// unit (b, kvh).  Thread t owns the contiguous pages [t per, t per + per) of
+// each window.  Every global load is issued up front (sequence length, the
+// first window's page-table entries, the thread's first selection entries),
+// then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
+// a block scan of the page flags, and one 32-byte store per tile.
+// s_flag: window ints, s_mask: 4 window words, scan_tmp: 32 ints.
+template <int NT>
 __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh, const int* __restrict__ seq_lens,
-                                                 const int* __restrict__ page_table,
-                                                 const int* sel_idx, const int* sel_cnt,
-                                                 int gran, Tile* __restrict__ tiles, int* __restrict__ ntiles,
-                                                 float* __restrict__ out, float* __restrict__ lse, int* status,
-                                                 int* flag, int* scan_tmp) {
+                                                 const int* __restrict__ page_table, const int* sel_idx,
+                                                 const int* sel_cnt, int gran, Tile* __restrict__ tiles,
+                                                 int* __restrict__ ntiles, float* __restrict__ out,
+                                                 float* __restrict__ lse, int* status, int* s_flag, uint32_t* s_mask,
+                                                 int* scan_tmp) {
+  constexpr int kPer = (kWinPages + NT - 1) / NT;   // pages per thread and window, at most
+  constexpr int kItemRegs = 2;                      // selection entries prefetched per thread (r = 0, 1 below)
+  auto bsync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); };
   const int u = b * p.Hk + kvh;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
-  const int Lc = max(0, min(seq_lens[b], p.mpp * kP));
+  const int* pt_row = page_table + (size_t)b * p.mpp;
+  const int win = min(p.mpp, kWinPages);
+  const int per = (win + NT - 1) / NT;
+  // ---- up-front loads
+  const int Lraw = seq_lens[b];
+  int ptr[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int i = tid * per + r;
+    ptr[r] = (r < per && i < win) ? __ldg(pt_row + i) : -1;
+  }
+  const int nitems = G * p.kcap;
+  int icnt[kItemRegs], iidx[kItemRegs];
+#pragma unroll
+  for (int r = 0; r < kItemRegs; ++r) {
+    const int it = tid + r * NT;
+    icnt[r] = 0;
+    iidx[r] = 0;
+    if (it < nitems) {
+      const int g = it / p.kcap, i = it - g * p.kcap;
+      const int h = kvh * G + g;
+      icnt[r] = sel_cnt[(size_t)b * p.Hq + h];
+      iidx[r] = sel_idx[((size_t)b * p.Hq + h) * p.kcap + i];
+    }
+  }
+  const int Lc = max(0, min(Lraw, p.mpp * kP));
   const int npg = (Lc + kP - 1) / kP;
   int s_end, w_beg;
   partition(Lc, p.S, p.W, s_end, w_beg);
   const int Bs = p.bs[kvh];
-  Tile* T = tiles + (size_t)u * p.mpp;
-
-  for (int i = tid; i < npg; i += blockDim.x) {
-    const int t0 = i * kP, t1 = t0 + kP;
-    flag[i] = (t0 < s_end) || (t1 > w_beg);   // page meets I
-  }
-  __syncthreads();
-  const int nitems = G * p.kcap;
-  for (int it = tid; it < nitems; it += blockDim.x) {
-    const int g = it / p.kcap, i = it % p.kcap;
-    const int h = kvh * G + g;
-    const int cnt = min(sel_cnt[(size_t)b * p.Hq + h], p.kcap);
-    if (i >= cnt) continue;
-    int lo, hi;
-    item_range(gran, sel_idx[((size_t)b * p.Hq + h) * p.kcap + i], Bs, Lc, s_end, w_beg, lo, hi);
-    for (int pg = lo / kP; lo < hi && pg <= (hi - 1) / kP; ++pg) flag[pg] = 1;
-  }
-  __syncthreads();
-
-  // exclusive scan of the page flags -> tile index (contiguous ranges per thread)
-  const int per = (npg + blockDim.x - 1) / blockDim.x;
-  const int a = min(npg, tid * per), e = min(npg, a + per);
-  int c = 0;
-  for (int i = a; i < e; ++i) c += flag[i];
-  int x = c;
-  const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scan_tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? scan_tmp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < nw) scan_tmp[lane] = w;
-  }
-  __syncthreads();
-  int base = (warp > 0 ? scan_tmp[warp - 1] : 0) + x - c;
-  const int total = scan_tmp[nw - 1];
   const uint32_t all = (1u << G) - 1u;
-  for (int i = a; i < e; ++i) {
-    if (flag[i]) flag[i] = base++;
-    else flag[i] = -1;
-  }
-  __syncthreads();
-  // descriptors: page-table loads of 4 pages are in flight together
-  for (int i0 = tid; i0 < npg; i0 += 4 * blockDim.x) {
-    int ph[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = i0 + k * blockDim.x;
-      ph[k] = (i < npg && flag[i] >= 0) ? __ldg(page_table + (size_t)b * p.mpp + i) : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = i0 + k * blockDim.x;
-      if (i < npg && flag[i] >= 0) {
-        Tile t;
-        t.lp = i;
-        const bool ok = ph[k] >= 0 && ph[k] < p.num_pages;
-        if (!ok) set_status(status, SA_ERR_BAD_PAGE);
-        t.phys = ok ? ph[k] : -1;
-        t.pad[0] = t.pad[1] = 0;
-        // dense-set tokens of this page attend for every head
-#pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int tok = i * kP + 4 * w4 + r;
-            if (tok < Lc && (tok < s_end || tok >= w_beg)) m |= all << (8 * r);
-          }
-          t.mask[w4] = m;
-        }
-        T[flag[i]] = t;
-      }
-    }
-  }
-  __syncthreads();
+  Tile* T = tiles + (size_t)u * p.mpp;
+  int total = 0;
 
-  // OR in each head's selected tokens inside M
-  for (int it = tid; it < nitems; it += blockDim.x) {
-    const int g = it / p.kcap, i = it % p.kcap;
-    const int h = kvh * G + g;
-    const int cnt = min(sel_cnt[(size_t)b * p.Hq + h], p.kcap);
-    if (i >= cnt) continue;
-    int lo, hi;
-    item_range(gran, sel_idx[((size_t)b * p.Hq + h) * p.kcap + i], Bs, Lc, s_end, w_beg, lo, hi);
-    for (int tok = lo; tok < hi;) {
-      const int pg = tok / kP;
-      const int r0 = tok % kP;
-      const int r1 = min(kP, r0 + (hi - tok));
-      Tile* t = T + flag[pg];
-      // rows [r0, r1) of this page get bit g
-      for (int w4 = r0 >> 2; w4 <= (r1 - 1) >> 2; ++w4) {
+  for (int w0 = 0; w0 < npg; w0 += kWinPages) {
+    const int wn = min(kWinPages, npg - w0);
+    const int a = min(wn, tid * per), e = min(wn, a + per);
+    // dense-set tokens of each page attend for every head
+    for (int i = a; i < e; ++i) {
+      uint32_t any = 0;
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t m = 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int row = 4 * w4 + r;
-          if (row >= r0 && row < r1) m |= (1u << g) << (8 * r);
+          const int tok = (w0 + i) * kP + 4 * w4 + r;
+          if (tok < Lc && (tok < s_end || tok >= w_beg)) m |= all << (8 * r);
         }
-        atomicOr(&t->mask[w4], m);
+        s_mask[4 * i + w4] = m;
+        any |= m;
       }
-      tok += r1 - r0;
+      s_flag[i] = any != 0;
     }
+    bsync();
+    // each head's selected tokens inside M (and inside this window)
+    const int tlo = w0 * kP, thi = (w0 + wn) * kP;
+    for (int it = tid, r = 0; it < nitems; it += NT, ++r) {
+      const int g = it / p.kcap, i = it - g * p.kcap;
+      int cnt, x;
+      if (r == 0) {
+        cnt = icnt[0];
+        x = iidx[0];
+      } else if (r == 1) {
+        cnt = icnt[1];
+        x = iidx[1];
+      } else {
+        const int h = kvh * G + g;
+        cnt = sel_cnt[(size_t)b * p.Hq + h];
+        x = sel_idx[((size_t)b * p.Hq + h) * p.kcap + i];
+      }
+      if (i >= min(cnt, p.kcap)) continue;
+      int lo, hi;
+      item_range(gran, x, Bs, Lc, s_end, w_beg, lo, hi);
+      lo = max(lo, tlo);
+      hi = min(hi, thi);
+      for (int tok = lo; tok < hi;) {
+        const int pg = tok / kP - w0;
+        const int r0 = tok % kP;
+        const int r1 = min(kP, r0 + (hi - tok));
+        for (int w4 = r0 >> 2; w4 <= (r1 - 1) >> 2; ++w4) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int row = 4 * w4 + rr;
+            if (row >= r0 && row < r1) m |= (1u << g) << (8 * rr);
+          }
+          atomicOr(&s_mask[4 * pg + w4], m);
+        }
+        s_flag[pg] = 1;
+        tok += r1 - r0;
+      }
+    }
+    bsync();
+    // exclusive scan of the page flags over the threads' contiguous ranges
+    int c = 0;
+    for (int i = a; i < e; ++i) c += s_flag[i];
+    const int x = warp_incl_scan(c);
+    if (lane == 31) scan_tmp[warp] = x;
+    bsync();
+    if (warp == 0) {
+      const int y = warp_incl_scan(lane < NT / 32 ? scan_tmp[lane] : 0);
+      if (lane < NT / 32) scan_tmp[lane] = y;
+    }
+    bsync();
+    int idx = total + (warp > 0 ? scan_tmp[warp - 1] : 0) + x - c;
+    // one 32-byte descriptor per tile (the page-table entry prefetched when possible)
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = a + r;
+      if (r < per && i < e && s_flag[i]) {
+        const int ph = w0 == 0 ? ptr[r] : __ldg(pt_row + w0 + i);
+        const bool ok = ph >= 0 && ph < p.num_pages;
+        if (!ok) set_status(status, SA_ERR_BAD_PAGE);
+        int4* dst = reinterpret_cast<int4*>(T + idx);
+        dst[0] = make_int4(w0 + i, ok ? ph : -1, 0, 0);
+        dst[1] = make_int4((int)s_mask[4 * i], (int)s_mask[4 * i + 1], (int)s_mask[4 * i + 2], (int)s_mask[4 * i + 3]);
+        ++idx;
+      }
+    }
+    total += scan_tmp[NT / 32 - 1];
+    bsync();   // the window's shared state is reused by the next window
   }
   if (tid == 0) ntiles[u] = total;
   if (total == 0) {   // nothing attended (L = 0): O = 0, lse = -inf; the decode kernel skips the unit
-    for (int i = tid; i < G * kD; i += blockDim.x) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
+    for (int i = tid; i < G * kD; i += NT) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
     if (tid < G) lse[(size_t)b * p.Hq + kvh * G + tid] = -INFINITY;
   }
 }
