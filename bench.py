@@ -50,6 +50,25 @@ def dist_info():
     return ws, rank, local
 
 
+STEP_LAUNCHES = 5   # kernels of one sa_decode_step: scores, top-k, tile build + tail summary, decode, chunk merge
+
+
+def reduce_max_ms(ms, world, device):
+    """Maximum over the ranks of a per-rank duration; every rank gets it."""
+    if world == 1:
+        return float(ms)
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, queries_per_step, steps, max_ms):
+    """Queries per second of the whole job: every rank decodes its own batch
+    each step (replicas), timed by the slowest rank."""
+    return world * queries_per_step * steps / (max_ms / 1e3)
+
+
 def measured_hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -262,14 +281,10 @@ def run_ours(args):
     clk = clocks.stop()
     dec_ms = [dec_total / K]
     sel_ms = [sel_total / K]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(total_ms, world, dev)
     ms_step = total_ms / K
     queries = wl.B * wl.Hq
-    value = world * queries * K / (total_ms / 1e3)
+    value = whole_job_value(world, queries, K, total_ms)
 
     layer_of = [(W + i) % N_LAYERS for i in range(K)]
     dec_bytes = float(np.mean([nbytes[l]["decode"] for l in layer_of]))
@@ -280,7 +295,7 @@ def run_ours(args):
 
     # end to end through the public binding: pinned host q in, O + lse out
     e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
-    gpu_launches = 4 * K
+    gpu_launches = STEP_LAUNCHES * K
 
     res = {
         "metric": METRIC,

@@ -175,8 +175,9 @@ int sa_select_topk(const sa_problem* prob, const void* q,
  *   out[b][h][:] = sum_t softmax(z)_t v_t  (fp32), lse[b][h] = log sum e^{z_t}.
  * Entries outside M or beyond L are ignored; duplicates count once.  The KV
  * rows of the union over a KV head's G query heads are read once.  Work is
- * split into chunks whose partial (max, sum, O) are combined with the
- * identity above by the last chunk to finish.  An empty attended set (L = 0)
+ * split into chunks of pages whose partials (max, sum, O) are combined with
+ * the identity above, in chunk order, by a second kernel on the same stream
+ * (no host synchronisation).  An empty attended set (L = 0)
  * gives out = 0, lse = -inf.
  * sel_granularity: SA_SEL_BLOCK (entries are blocks of the KV head's Bs) or
  *   SA_SEL_TOKEN (entries are positions).

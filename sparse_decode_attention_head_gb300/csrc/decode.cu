@@ -6,29 +6,33 @@
 // and selected older entries sparsely and fuses the two partial outputs with
 //   O = (e^lse_I O_I + e^lse_J O_J) / (e^lse_I + e^lse_J).
 // The identity holds for any partition, so here the attended rows of one KV
-// head are cut into chunks of whole pages, each chunk keeps a running
-// (max, sum, O) per query head, and the last chunk to finish merges all
-// chunk partials with the same identity (stabilised by the maximum, as the
-// review's comment on Sec. 3.3 asks).
+// head are cut into chunks of whole pages, each chunk leaves a partial
+// (max, sum, unnormalised O) per query head, and the chunks of a unit are
+// merged with the same identity, in chunk order, stabilised by the running
+// maximum (the review's comment on Sec. 3.3).
 //
 // Kernel 1 (tile builder, one CTA per (sequence, KV head)): the union over
 // the G query heads of the pages to read, as an ascending list of tiles; a
 // tile is one 16-token page with a G-bit head mask per token, so the rows a
 // GQA group shares are read once (SPIN abstract / Fig. 6: paged KV substrate).
 //
-// Kernel 2 (decode, persistent, stream-K): the tile lists of all units are
-// concatenated and every CTA takes an equal contiguous slice, so the load is
-// balanced whatever the union sizes are.  A producer warp keeps a ring of
-// page slots full (one lane per slot, each running on its own): it reads the
-// tile descriptor (the builder already looked the page up) and issues 2-D TMA
-// loads (SWIZZLE_128B, two 16 x 64 bf16 boxes per 4 KB slab of K and of V)
-// that complete on the slot's "full" mbarrier.  Consumer warps take the slice's
-// tiles round-robin: S = K Q^T and O^T += V^T P on mma.sync m16n8k16 (tokens x
-// heads, heads padded to 8), with P split into a bf16 high part and a bf16
-// residual so the product keeps ~16 mantissa bits; they release the slot on
-// its "empty" mbarrier.  At the end of each unit segment the consumer warps
-// merge their states; a unit split over several CTAs leaves one partial per
-// CTA, and the last CTA to finish merges them in CTA order (deterministic).
+// Kernel 2 (decode, persistent, dynamically scheduled): the tile lists are cut
+// into chunks of C tiles that never cross a unit; CTA c starts on chunk c and
+// takes further chunks from a global ticket counter, so CTAs whose pages land
+// faster take more chunks.  A producer warp keeps a ring of page slots full
+// (one lane per slot): it reads the tile descriptor (the builder already
+// looked the page up) and issues 2-D TMA loads (SWIZZLE_128B, two 16 x 64
+// bf16 boxes per 4 KB slab of K and of V) that complete on the slot's "full"
+// mbarrier.  Consumer warps take the landed slots of their current chunk:
+// S = K Q^T and O^T += V^T P on mma.sync m16n8k16 (tokens x heads, heads
+// padded to 8), with P split into a bf16 high part and a bf16 residual so the
+// product keeps ~16 mantissa bits; they release the slot on its "empty"
+// mbarrier.  A warp that has done its share of a chunk parks its state and
+// moves on; the last warp to park combines the four states into the chunk
+// partial.
+//
+// Kernel 3 (merge, one CTA per (query head, unit)): the chain merge of the
+// unit's chunk partials.  Units held in one chunk are finished by kernel 2.
 #include <cuda.h>
 
 #include <algorithm>
