@@ -3,7 +3,9 @@
 // threads (a whole block, or a slice of one with its own named barrier)
 // holds KPT consecutive keys per thread in registers, finds the k-th key by
 // an MSB-first radix select over order-preserving uint32 keys (starting below
-// the bits every key shares), and compacts in index order.
+// the bits every key shares; once the bucket holding the k-th key has at most
+// 32 keys, one warp finds the k-th key among them directly), and compacts in
+// index order.
 #pragma once
 
 #include "sa_common.cuh"
@@ -23,8 +25,11 @@ __device__ __forceinline__ void group_sync(int id, int n) {
 struct TopkScratch {
   int hist[256];
   int red[2][32];
+  uint32_t cand[32];   // keys of a small last bucket
   uint32_t prefix;
   int krem;
+  int bcnt;            // keys in the bucket holding the k-th key
+  int nc;              // keys gathered into cand
 };
 
 // Exclusive scan over the group; tmp holds >= GROUP / 32 ints.
@@ -99,15 +104,46 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
           if (above < krem && krem <= above + cnt[q]) {
             S.prefix = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
             S.krem = krem - above;
+            S.bcnt = cnt[q];
           }
           above += cnt[q];
         }
       }
     }
+    if (tg == 0) S.nc = 0;
     group_sync(bar_id, GROUP);
     prefix = S.prefix;
     krem = S.krem;
     mask |= dmask << shift;
+    if (shift > 0 && S.bcnt <= 32) {
+      // gather the bucket and let warp 0 rank its keys: the krem-th largest is T
+#pragma unroll
+      for (int q = 0; q < KPT; ++q) {
+        const int i = tg * KPT + q;
+        if (i < n && (key[q] & mask) == prefix) S.cand[atomicAdd(&S.nc, 1)] = key[q];
+      }
+      group_sync(bar_id, GROUP);
+      if (w == 0) {
+        const int nc = S.nc;
+        const uint32_t mine = lane < nc ? S.cand[lane] : 0u;
+        int gt_cnt = 0, ge_cnt = 0;
+        for (int j = 0; j < nc; ++j) {
+          const uint32_t o = __shfl_sync(0xffffffffu, mine, j);
+          gt_cnt += o > mine;
+          ge_cnt += o >= mine;
+        }
+        if (lane < nc && gt_cnt < krem && krem <= ge_cnt) {   // every lane holding T agrees
+          S.prefix = mine;
+          S.krem = krem - gt_cnt;
+        }
+      }
+      group_sync(bar_id, GROUP);
+      prefix = S.prefix;
+      krem = S.krem;
+      mask = 0xffffffffu;
+      group_sync(bar_id, GROUP);
+      break;
+    }
     group_sync(bar_id, GROUP);
   }
   const uint32_t T = prefix;   // key of the k-th best
