@@ -50,7 +50,9 @@ def dist_info():
     return ws, rank, local
 
 
-STEP_LAUNCHES = 5   # kernels of one sa_decode_step: scores, top-k, tile build + tail summary, decode, chunk merge
+# kernels of one sa_decode_step on this workload: scores, fused top-k + tile build + tail summary,
+# decode, chunk merge
+STEP_LAUNCHES = 4
 
 
 def reduce_max_ms(ms, world, device):

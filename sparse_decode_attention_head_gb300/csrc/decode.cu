@@ -69,7 +69,9 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
   extern __shared__ int smem_b[];   // build_smem_bytes(mpp): window flags, then window masks
   __shared__ int scan_tmp[32];
   const int win = min(p.mpp, kWinPages);
-  build_unit_tiles<kBuildThreads>(p, blockIdx.y, blockIdx.x, seq_lens, page_table, sel_idx, sel_cnt, gran, tiles,
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
+  build_unit_tiles<kBuildThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0, gran, tiles,
                                   ntiles, out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win),
                                   scan_tmp);
 }

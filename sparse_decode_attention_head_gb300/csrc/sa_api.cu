@@ -51,6 +51,9 @@ int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
                       int* status, int* ticket, cudaStream_t stream);
+int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
+                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
+                        float* out, float* lse, int* status, int* ticket, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -321,9 +324,14 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
   int* status = at<int>(ws, l.header);
   float* scores = at<float>(ws, l.scores);
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
-  if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
-  rc = sa::launch_build_step(p, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt, at<void>(ws, l.tiles),
-                             at<int>(ws, l.ntiles), out, lse, status, at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
+  int* ticket = at<int>(ws, l.counters) + p.B * p.Hk + 1;
+  rc = sa::launch_select_build(p, scores, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt,
+                               at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+  if (rc == SA_ERR_UNSUPPORTED) {   // candidates beyond the fused kernel's capacity: two kernels
+    if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
+    rc = sa::launch_build_step(p, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt, at<void>(ws, l.tiles),
+                               at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+  }
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
                            at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);

@@ -13,6 +13,7 @@
 #include "sa_common.cuh"
 #include "summary.cuh"
 #include "tiles.cuh"
+#include "topk.cuh"
 
 namespace sa {
 
@@ -40,8 +41,10 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
     return;
   }
   const int win = min(p.mpp, kWinPages);
-  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx, sel_cnt, SA_SEL_BLOCK, tiles, ntiles,
-                                     out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
+  const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
+  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0,
+                                     SA_SEL_BLOCK, tiles, ntiles, out, lse, status, smem_b,
+                                     reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
 }
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
@@ -52,6 +55,82 @@ int launch_build_step(const Params& p, const int* seq_lens, const int* page_tabl
     cudaFuncSetAttribute(build_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
                                    seq_lens, page_table, static_cast<const __nv_bfloat16*>(k_pool),
+                                   static_cast<__nv_bfloat16*>(summ), sel_idx, sel_cnt, static_cast<Tile*>(tiles),
+                                   ntiles, out, lse, status, ticket);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ fused
+
+// One CTA per (sequence, KV head): the top-k of the group's G query heads
+// (head g on threads [g GROUP, (g + 1) GROUP), named barrier 1 + g, the
+// selections kept in shared memory), then the tile list of their union
+// (warps 0..30) and the tail summary (warp 31), as build_step_kernel.  It
+// replaces topk_kernel + build_step_kernel when every head's candidates fit
+// GROUP x KPT keys.
+template <int GROUP, int KPT>
+__global__ void __launch_bounds__(kStepBuildThreads)
+select_build_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
+                    const int* __restrict__ page_table, const __nv_bfloat16* __restrict__ k_pool,
+                    __nv_bfloat16* __restrict__ summ, int* __restrict__ sel_idx, int* __restrict__ sel_cnt,
+                    Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
+                    float* __restrict__ lse, int* status, int* ticket) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
+  extern __shared__ int smem_b[];   // window flags, window masks, then selections [G][kcap] and counts [G]
+  __shared__ TopkScratch S[kStepBuildThreads / GROUP];
+  __shared__ int scan_tmp[32];
+  const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int G = p.G;
+  const int win = min(p.mpp, kWinPages);
+  int* s_sel = smem_b + 5 * win;
+  int* s_cnt = s_sel + G * p.kcap;
+  const int L = min(seq_lens[b], p.mpp * kP);
+  int j0, j1;
+  candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+  const int g = tid / GROUP;
+  if (g < G) {
+    const int h = kvh * G + g;
+    group_topk<GROUP, KPT>(scores + ((size_t)b * p.Hq + h) * p.slots + j0, j1 - j0, p.k[h], j0,
+                           s_sel + g * p.kcap, s_cnt + g, 1 + g, S[g]);
+  }
+  __syncthreads();
+  const size_t h0 = (size_t)b * p.Hq + kvh * G;
+  for (int i = tid; i < G * p.kcap; i += kStepBuildThreads)
+    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
+  if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
+  if (tid >= kStepTileThreads) {
+    if (L > 0)
+      summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
+    return;
+  }
+  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, s_sel, s_cnt, SA_SEL_BLOCK, tiles, ntiles, out,
+                                     lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
+}
+
+// SA_ERR_UNSUPPORTED when some head's candidates exceed the fused kernel's
+// key capacity or its shared memory would not fit; the caller then runs
+// topk_kernel + build_step_kernel.
+int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
+                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
+                        float* out, float* lse, int* status, int* ticket, cudaStream_t stream) {
+  int max_n = 0;
+  for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  const size_t smem = build_smem_bytes(p.mpp) + ((size_t)p.G * p.kcap + p.G) * sizeof(int);
+  if (smem > 160 * 1024) return SA_ERR_UNSUPPORTED;
+  void (*kern)(Params, const float*, const int*, const int*, const __nv_bfloat16*, __nv_bfloat16*, int*, int*,
+               Tile*, int*, float*, float*, int*, int*) = nullptr;
+  if (p.G <= 4) {
+    if (max_n <= 256 * 8) kern = select_build_kernel<256, 8>;
+    else if (max_n <= 256 * 16) kern = select_build_kernel<256, 16>;
+  } else {
+    if (max_n <= 128 * 16) kern = select_build_kernel<128, 16>;
+  }
+  if (kern == nullptr) return SA_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = launch_pdl(kern, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p, scores, seq_lens,
+                                   page_table, static_cast<const __nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(summ), sel_idx, sel_cnt, static_cast<Tile*>(tiles),
                                    ntiles, out, lse, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;

@@ -42,11 +42,13 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
 // first window's page-table entries, the thread's first selection entries),
 // then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
 // a block scan of the page flags, and one 32-byte store per tile.
-// s_flag: window ints, s_mask: 4 window words, scan_tmp: 32 ints.
+// sel_row: the unit's selections [G][kcap] (global or shared memory),
+// cnt_row: their counts [G].  s_flag: window ints, s_mask: 4 window words,
+// scan_tmp: 32 ints.
 template <int NT>
 __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh, const int* __restrict__ seq_lens,
-                                                 const int* __restrict__ page_table, const int* sel_idx,
-                                                 const int* sel_cnt, int gran, Tile* __restrict__ tiles,
+                                                 const int* __restrict__ page_table, const int* sel_row,
+                                                 const int* cnt_row, int gran, Tile* __restrict__ tiles,
                                                  int* __restrict__ ntiles, float* __restrict__ out,
                                                  float* __restrict__ lse, int* status, int* s_flag, uint32_t* s_mask,
                                                  int* scan_tmp) {
@@ -75,10 +77,9 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
     icnt[r] = 0;
     iidx[r] = 0;
     if (it < nitems) {
-      const int g = it / p.kcap, i = it - g * p.kcap;
-      const int h = kvh * G + g;
-      icnt[r] = sel_cnt[(size_t)b * p.Hq + h];
-      iidx[r] = sel_idx[((size_t)b * p.Hq + h) * p.kcap + i];
+      const int g = it / p.kcap;
+      icnt[r] = cnt_row[g];
+      iidx[r] = sel_row[it];
     }
   }
   const int Lc = max(0, min(Lraw, p.mpp * kP));
@@ -122,9 +123,8 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
         cnt = icnt[1];
         x = iidx[1];
       } else {
-        const int h = kvh * G + g;
-        cnt = sel_cnt[(size_t)b * p.Hq + h];
-        x = sel_idx[((size_t)b * p.Hq + h) * p.kcap + i];
+        cnt = cnt_row[g];
+        x = sel_row[it];
       }
       if (i >= min(cnt, p.kcap)) continue;
       int lo, hi;
