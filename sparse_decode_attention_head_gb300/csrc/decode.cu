@@ -336,10 +336,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               uint8_t* dst = s_tiles + (size_t)slot * kTileBytes;
               const int row = (phys * p.Hk + (ci.unit % p.Hk)) * kP;
               mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
-              tma_load_2d(dst, &tmK, 0, row, &s_full[slot]);
-              tma_load_2d(dst + kBoxBytes, &tmK, 64, row, &s_full[slot]);
-              tma_load_2d(dst + kSlab, &tmV, 0, row, &s_full[slot]);
-              tma_load_2d(dst + kSlab + kBoxBytes, &tmV, 64, row, &s_full[slot]);
+              tma_load_3d(dst, &tmK, 0, row, 0, &s_full[slot]);
+              tma_load_3d(dst + kSlab, &tmV, 0, row, 0, &s_full[slot]);
             } else {
               mbar_arrive(&s_full[slot]);
             }

@@ -158,11 +158,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int make_kv_map(CUtensorMap* m, const void* pool, const Params& p) {
   auto fn = encode_fn();
   if (fn == nullptr) return SA_ERR_CUDA;
-  cuuint64_t dims[2] = {(cuuint64_t)SA_HEAD_DIM, (cuuint64_t)p.num_pages * p.Hk * SA_PAGE_SIZE};
-  cuuint64_t strides[1] = {(cuuint64_t)SA_HEAD_DIM * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+  // the pool as (64 dims, rows, 2 halves of a row): one box of 64 x 16 x 2
+  // is a whole 4 KB page slab, landing as [half][row][64] with the 128-byte
+  // swizzle, the layout two 64 x 16 boxes of a 2-D map would give
+  cuuint64_t dims[3] = {64, (cuuint64_t)p.num_pages * p.Hk * SA_PAGE_SIZE, 2};
+  cuuint64_t strides[2] = {(cuuint64_t)SA_HEAD_DIM * 2, 128};
+  cuuint32_t box[3] = {64, 16, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
