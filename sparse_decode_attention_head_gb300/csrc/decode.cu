@@ -725,7 +725,7 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
                        int* ticket, cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(build_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    smem_limit_at_least(reinterpret_cast<const void*>(build_tiles_kernel), (int)smem);
   dim3 grid(p.Hk, p.B);
   const cudaError_t e = launch_pdl(build_tiles_kernel, grid, dim3(kBuildThreads), smem, stream, p, seq_lens,
                                    page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, out, lse,
@@ -740,11 +740,8 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   const int nslots = decode_slots(U, p.G);
   const size_t smem = decode_smem_bytes_n(U, p.G, nslots);
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
-  cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kDecThreads, smem) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  smem_limit_at_least(reinterpret_cast<const void*>(decode_kernel), (int)smem);
+  const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(decode_kernel), kDecThreads, smem);
   const int grid = std::min(kMaxCtas, num_sms * per_sm);
   DecodeArgs A;
   A.q = static_cast<const __nv_bfloat16*>(q);

@@ -155,7 +155,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Pool [num_pages][Hk][P][D] bf16 viewed as rows of D; boxes of 16 rows x 64.
+int encode_kv_map(CUtensorMap* m, const void* pool, const Params& p);
+
+// The last few maps a host thread encoded, keyed by pool address, shape and
+// device: a decode step needs two, and encoding is host work worth skipping.
 int make_kv_map(CUtensorMap* m, const void* pool, const Params& p) {
+  struct Entry {
+    const void* pool;
+    int num_pages, Hk, dev;
+    CUtensorMap map;
+  };
+  thread_local Entry cache[8] = {};
+  thread_local int next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  for (const Entry& e : cache)
+    if (e.pool == pool && pool != nullptr && e.num_pages == p.num_pages && e.Hk == p.Hk && e.dev == dev) {
+      *m = e.map;
+      return SA_OK;
+    }
+  const int rc = encode_kv_map(m, pool, p);
+  if (rc == SA_OK) {
+    cache[next] = Entry{pool, p.num_pages, p.Hk, dev, *m};
+    next = (next + 1) % 8;
+  }
+  return rc;
+}
+
+int encode_kv_map(CUtensorMap* m, const void* pool, const Params& p) {
   auto fn = encode_fn();
   if (fn == nullptr) return SA_ERR_CUDA;
   // the pool as (64 dims, rows, 2 halves of a row): one box of 64 x 16 x 2

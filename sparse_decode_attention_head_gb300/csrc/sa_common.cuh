@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
 #include <utility>
 
 #include "sa.h"
@@ -79,6 +81,39 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // own pdl_wait(), so stream order is kept and only the launch gap overlaps.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host side, once per (kernel, device): raise the kernel's dynamic
+// shared-memory limit to at least `bytes`, and the resident CTAs per SM at a
+// given shared-memory size.  Both are runtime round trips not worth paying on
+// every launch.
+inline cudaError_t smem_limit_at_least(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
+}
+
+inline int ctas_per_sm(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<std::pair<const void*, int>, size_t>, int> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_pair(std::make_pair(kernel, dev), smem);
+  const auto it = done.find(key);
+  if (it != done.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+  done[key] = n;
+  return n;
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

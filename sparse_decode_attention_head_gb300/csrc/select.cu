@@ -259,13 +259,13 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
 #define SA_SCORE_CASE(GG)                                                                         \
   case GG:                                                                                        \
     if (p.mode == SA_SUMMARY_MINMAX) {                                                            \
-      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MINMAX>,                                   \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+      smem_limit_at_least(reinterpret_cast<const void*>(score_kernel<GG, SA_SUMMARY_MINMAX>),     \
+                          (int)smem);                                                             \
       err = launch_pdl(score_kernel<GG, SA_SUMMARY_MINMAX>, dim3(grid), dim3((kScoreWarps + 1) * 32), \
                        smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
     } else {                                                                                      \
-      cudaFuncSetAttribute(score_kernel<GG, SA_SUMMARY_MEAN>,                                     \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+      smem_limit_at_least(reinterpret_cast<const void*>(score_kernel<GG, SA_SUMMARY_MEAN>),       \
+                          (int)smem);                                                             \
       err = launch_pdl(score_kernel<GG, SA_SUMMARY_MEAN>, dim3(grid), dim3((kScoreWarps + 1) * 32),   \
                        smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
     }                                                                                             \

@@ -143,6 +143,7 @@ class Problem:
         self.k_per_head = list(k_per_head)
         self._bs = (ctypes.c_int32 * max(1, len(self.block_sizes)))(*self.block_sizes)
         self._k = (ctypes.c_int32 * max(1, len(self.k_per_head)))(*self.k_per_head)
+        self._summary_shape = None
         self._c = _Problem(B, Hq, Hk, D, page_size, max_pages_per_seq, num_pages, sink, window, mode,
                            ctypes.cast(self._bs, ctypes.POINTER(ctypes.c_int32)),
                            ctypes.cast(self._k, ctypes.POINTER(ctypes.c_int32)), kcap, self.scale)
@@ -162,10 +163,13 @@ class Problem:
         return int(lib().sa_workspace_size(self.ref))
 
     def summary_shape(self):
-        s = self.block_slots()
-        if self.mode == SUMMARY_MINMAX:
-            return (self.B, self.Hk, s, 2, self.D)
-        return (self.B, self.Hk, s, self.D)
+        if self._summary_shape is None:
+            s = self.block_slots()
+            if self.mode == SUMMARY_MINMAX:
+                self._summary_shape = (self.B, self.Hk, s, 2, self.D)
+            else:
+                self._summary_shape = (self.B, self.Hk, s, self.D)
+        return self._summary_shape
 
 
 class Workspace:
@@ -267,10 +271,7 @@ def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, s
         _stream()), "sa_update_score_tables")
 
 
-def decode_step(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse,
-                ws: Workspace):
-    """Whole block-selection decode step: tail-block summary refresh, scores,
-    top-k and the paged sparse decode (sa_decode_step)."""
+def _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse):
     _need(q, torch.bfloat16, "q", (prob.B, prob.Hq, prob.D))
     _need(k_pool, torch.bfloat16, "k_pool")
     _need(v_pool, torch.bfloat16, "v_pool", tuple(k_pool.shape))
@@ -281,6 +282,33 @@ def decode_step(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summarie
     _need(sel_cnt, torch.int32, "sel_cnt", (prob.B, prob.Hq))
     _need(out, torch.float32, "out", (prob.B, prob.Hq, prob.D))
     _need(lse, torch.float32, "lse", (prob.B, prob.Hq))
+
+
+def decode_step(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse,
+                ws: Workspace):
+    """Whole block-selection decode step: tail-block summary refresh, scores,
+    top-k and the paged sparse decode (sa_decode_step)."""
+    _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse)
     _check(lib().sa_decode_step(prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens),
                                 _ptr(summaries), _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf),
                                 _stream()), "sa_decode_step")
+
+
+class DecodeStepCall:
+    """sa_decode_step bound to fixed tensors: the arguments are checked and
+    marshalled once, each call passes only the current stream.  The tensors'
+    contents may change between calls (a serving loop that reuses its
+    buffers); the object keeps them alive."""
+
+    def __init__(self, prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out,
+                 lse, ws: Workspace):
+        _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse)
+        self._keep = (prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse, ws)
+        self._fn = lib().sa_decode_step
+        self._args = (prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens),
+                      _ptr(summaries), _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf))
+
+    def __call__(self):
+        rc = self._fn(*self._args, _stream())
+        if rc != SA_OK:
+            raise SAError(rc, "sa_decode_step")

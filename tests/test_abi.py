@@ -76,3 +76,15 @@ def test_status_strings(lib):
     for c in range(7):
         assert sa.status_string(c) not in ("", "unknown status")
     assert sa.status_string(99) == "unknown status"
+
+
+def test_prepared_step_call_checks_its_tensors_once():
+    """DecodeStepCall validates at construction (no GPU needed to reach the checks)."""
+    import pytest
+    import torch
+    from sparse_decode_attention_head_gb300 import sa
+    prob = sa.Problem(B=1, Hq=4, Hk=1, max_pages_per_seq=4, num_pages=4, sink=4, window=16, block_sizes=[16],
+                      k_per_head=[1] * 4, kcap=1)
+    cpu = torch.zeros(1, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        sa.DecodeStepCall(prob, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, None)

@@ -298,3 +298,34 @@ def test_decode_step_matches_separate_calls(name):
             assert torch.equal(idx[b, h, :n], idx_ref[b, h, :n])
     H.assert_close(out.cpu().numpy(), o_ref.cpu().numpy(), "step O")
     H.assert_close(lse.cpu().numpy(), l_ref.cpu().numpy(), "step lse")
+
+
+@pytest.mark.gpu
+def test_prepared_step_call_matches_decode_step():
+    # sa.DecodeStepCall marshals once and passes only the stream on each call;
+    # with fresh contents in the same buffers it gives decode_step's results
+    wl = synth.workload("tiny_4k")
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    ws = sa.Workspace(prob)
+    case = synth.make_decode_case(wl, 41)
+    dev = H.to_dev(case)
+    summ = H.gpu_summaries(prob, dev, ws)
+    idx = torch.empty(wl.B, wl.Hq, prob.kcap, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(wl.B, wl.Hq, dtype=torch.int32, device="cuda")
+    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.float32, device="cuda")
+    lse = torch.empty(wl.B, wl.Hq, dtype=torch.float32, device="cuda")
+    call = sa.DecodeStepCall(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ,
+                             idx, cnt, out, lse, ws)
+    for seed in (42, 43):
+        q_new = synth.make_decode_case(wl, seed).q.to("cuda")
+        dev["q"].copy_(q_new)
+        call()
+        o1, l1, i1, c1 = out.clone(), lse.clone(), idx.clone(), cnt.clone()
+        sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx,
+                       cnt, out, lse, ws)
+        torch.cuda.synchronize()
+        assert ws.status() == sa.SA_OK
+        assert torch.equal(c1, cnt) and torch.equal(i1, idx)
+        H.assert_close(o1.cpu().numpy(), out.cpu().numpy(), "prepared O")
+        H.assert_close(l1.cpu().numpy(), lse.cpu().numpy(), "prepared lse")
