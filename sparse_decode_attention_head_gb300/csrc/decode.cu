@@ -45,7 +45,7 @@ namespace sa {
 constexpr int kConsWarps = 4;                      // consumer warps
 constexpr int kDecThreads = (kConsWarps + 1) * 32; // + one producer warp
 constexpr int kMaxCtas = 512;                      // grid cap (partial slots are sized for it)
-constexpr int kChunksPerCta = 8;                   // chunk size: about this many chunks per CTA ...
+constexpr int kChunksPerCta = 3;                   // chunk size: about this many chunks per CTA ...
 constexpr int kMinChunk = 8;                       // ... but at least this many tiles
 constexpr int kChunkRing = 32;                     // published chunks not yet finished (> slots)
 constexpr int kMaxSlotsPerWarp = 4;                // slots <= 16
