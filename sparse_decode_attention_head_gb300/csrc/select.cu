@@ -198,29 +198,54 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
             for (int k2 = 0; k2 < 8; ++k2) xmin[k2] = 0u;
           }
         }
-        float res[HPW];
+        float acc[HPW];
 #pragma unroll
         for (int e = 0; e < HPW; ++e) {
-          float acc = 0.f;
+          float a = 0.f;
 #pragma unroll
           for (int k2 = 0; k2 < 8; ++k2) {
             const uint32_t w = (MODE == SA_SUMMARY_MINMAX) ? __byte_perm(xmax[k2], xmin[k2], selw[e][k2]) : xmax[k2];
             // fma with c = -0 is the plain product, zero signs included
-            acc = fma_bf16_lo(qw[e][k2], w, k2 == 0 ? -0.0f : acc);
-            acc = fma_bf16_hi(qw[e][k2], w, acc);
+            a = fma_bf16_lo(qw[e][k2], w, k2 == 0 ? -0.0f : a);
+            a = fma_bf16_hi(qw[e][k2], w, a);
           }
-          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
-          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
-          acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-          res[e] = __fadd_rn(acc, 0.0f);
+          acc[e] = a;
         }
-        // lane part e writes head hset * HPW + e
-        float v = res[0];
+        if (HPW == 4) {
+          // Butterfly over the parts with the heads spread over the lanes: at
+          // partner distance 4 a lane keeps two heads and sends the other
+          // two, at distance 2 it keeps one, at distance 1 both partners hold
+          // the same head.  Every add is (own partial) + (partner's partial)
+          // of one head, the sums of the plain per-head butterfly.
+          const bool b2 = (part & 4) != 0, b1 = (part & 2) != 0;
+          const float r0 = __shfl_xor_sync(0xffffffffu, b2 ? acc[0] : acc[2], 4);
+          const float r1 = __shfl_xor_sync(0xffffffffu, b2 ? acc[1] : acc[3], 4);
+          const float x0 = __fadd_rn(b2 ? acc[2] : acc[0], r0);   // head 2 b2
+          const float x1 = __fadd_rn(b2 ? acc[3] : acc[1], r1);   // head 2 b2 + 1
+          const float r2 = __shfl_xor_sync(0xffffffffu, b1 ? x0 : x1, 2);
+          const float y = __fadd_rn(b1 ? x1 : x0, r2);            // head 2 b2 + b1
+          const float z = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, 1));
+          const float v = __fadd_rn(z, 0.0f);
+          const int g = hset * HPW + (part >> 1);
+          if (valid && (part & 1) == 0 && g < G) scores[dsc.sbase + (long long)g * p.slots + cl] = v;
+        } else {
+          float res[HPW];
 #pragma unroll
-        for (int e = 1; e < HPW; ++e)
-          if (part == e) v = res[e];
-        const int g = hset * HPW + part;
-        if (valid && part < HPW && g < G) scores[dsc.sbase + (long long)g * p.slots + cl] = v;
+          for (int e = 0; e < HPW; ++e) {
+            float a = acc[e];
+            a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            res[e] = __fadd_rn(a, 0.0f);
+          }
+          // lane part e writes head hset * HPW + e
+          float v = res[0];
+#pragma unroll
+          for (int e = 1; e < HPW; ++e)
+            if (part == e) v = res[e];
+          const int g = hset * HPW + part;
+          if (valid && part < HPW && g < G) scores[dsc.sbase + (long long)g * p.slots + cl] = v;
+        }
       }
     }
     __syncwarp();
