@@ -297,6 +297,7 @@ def run_ours(args):
 
     # end to end through the public binding: pinned host q in, O + lse out
     e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
+    tables = None if args.no_tables else run_tables(args, dev)
     gpu_launches = STEP_LAUNCHES * K
 
     res = {
@@ -325,6 +326,7 @@ def run_ours(args):
                           "algorithmic_bytes_per_step": int(step_bytes),
                           "select_avg_ms": round(float(np.mean(sel_ms)), 5)},
         "e2e": e2e,
+        "tables_roofline": tables,
         "gpu_launches": gpu_launches,
         "clocks": clk,
     }
@@ -427,6 +429,74 @@ def run_e2e(args, prob, layers, ws, out, lse, dev):
                     "(O, lse) out copied on their own streams, overlapping the neighbouring steps"}
 
 
+def run_tables(args, dev, reps=100):
+    """Step a7 on the 128K table workload (B4, 32q/8kv, L 131072 + 1 per step):
+    sa_update_score_tables alone, in a CUDA graph of `reps` launches that
+    alternate the two table buffers, fed by one real decode step (its
+    selections, logits and lse).  The 4 x 64 MB tables and their 256 MB of
+    reads + writes per launch are larger than L2."""
+    wl = synth.table_workload("tables_128k")
+    case = synth.make_table_case(wl, 7, device=dev)
+    B, Hq, Hk = wl.B, wl.Hq, wl.Hk
+    mpp = wl.max_pages_per_seq
+    N = mpp * wl.P
+    prob = sa.Problem(B=B, Hq=Hq, Hk=Hk, max_pages_per_seq=mpp, num_pages=B * mpp, sink=wl.S, window=wl.W,
+                      block_sizes=[16] * Hk, k_per_head=[0] * Hq, kcap=wl.kcap)
+    ws = sa.Workspace(prob, device=dev)
+    tv = [case.vert0, torch.empty(B, Hq, N, device=dev)]
+    ts = [case.slash0, torch.empty(B, Hq, N, device=dev)]
+    cand = [torch.zeros(B, Hq, wl.kcap, dtype=torch.int32, device=dev) for _ in range(2)]
+    cnt = [torch.zeros(B, Hq, dtype=torch.int32, device=dev) for _ in range(2)]
+    logits = torch.zeros(B, Hq, N, device=dev)
+    out = torch.empty(B, Hq, wl.D, device=dev)
+    lse = torch.empty(B, Hq, device=dev)
+    L0 = wl.L0
+    sl0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
+    sl1 = torch.full((B,), L0 + 1, dtype=torch.int32, device=dev)
+    # one real step: first update (tables carried over), decode over I + candidates with logits
+    sa.update_score_tables(prob, tv[0], ts[0], tv[1], ts[1], sl0, cand[0], cnt[0], ws, beta=wl.beta)
+    sa.sparse_decode(prob, case.q_steps[0], case.k_pool, case.v_pool, case.page_table, sl0, cand[0], cnt[0], out,
+                     lse, ws, granularity=sa.SEL_TOKEN, logits=logits)
+    prev = dict(prev_seq_lens=sl0, prev_sel_idx=cand[0], prev_sel_cnt=cnt[0], prev_logits=logits, prev_lse=lse)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+
+    def update(i):
+        a, b = i % 2, (i + 1) % 2
+        sa.update_score_tables(prob, tv[b], ts[b], tv[a], ts[a], sl1, cand[1], cnt[1], ws, beta=wl.beta, prev=prev)
+
+    with torch.cuda.stream(st):
+        for i in range(3):
+            update(i)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=st, capture_error_mode="relaxed"):
+            for i in range(reps):
+                update(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    status = ws.status()
+    # algorithmic bytes: both tables read and written, the previous step's logits at
+    # its attended positions, its selection list, and the new candidate list
+    n_att = wl.S + wl.W + cnt[0].sum().item() / (B * Hq)
+    per_head = 4 * N * 4 + n_att * 4 + cnt[0].float().mean().item() * 4 + cnt[1].float().mean().item() * 4
+    nbytes = B * Hq * per_head
+    peak, peak_src = measured_hbm_peak()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "score tables, B4 x 32q/8kv heads, L 131072 + 1, tables fp32 [4][32][131136] x2",
+            "kernel": "sa_update_score_tables (decay, threshold, expansion in one pass)",
+            "avg_launch_ms": round(ms, 5), "algorithmic_bytes_per_launch": int(nbytes),
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "mean_candidates_per_head": round(cnt[1].float().mean().item(), 1), "status": status}
+
+
 # --------------------------------------------------------------------------- oracle timing
 
 def cpu_baseline(L, wl, ks, scale, budget_s=15.0, units=None):
@@ -496,6 +566,7 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="independent layer copies rotated per step (1.07 GB of KV each)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-tables", action="store_true", help="skip the score-table (a7) leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

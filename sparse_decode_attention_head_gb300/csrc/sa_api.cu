@@ -43,11 +43,15 @@ struct TableArgs {
   const int* lens;
   int* cand;
   int* cand_cnt;
+  int* stage;
+  int* stage_cnt;
   int* status;
   float decay;
   float beta;
 };
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
+size_t tables_stage_bytes(const Params& p);
+void tables_stage_ptrs(const Params& p, void* base, int** stage, int** cnt);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
                       int* status, int* ticket, cudaStream_t stream);
@@ -111,7 +115,7 @@ int make_params(const sa_problem* pr, Params* p) {
 }
 
 struct Layout {
-  size_t header, scores, tiles, ntiles, counters, partials, total;
+  size_t header, scores, tiles, ntiles, counters, partials, stage, total;
 };
 
 Layout layout_of(const Params& p) {
@@ -129,6 +133,8 @@ Layout layout_of(const Params& p) {
   off = align_up(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
   l.partials = off;
   off = align_up(off + sa::decode_partials_bytes(p));
+  l.stage = off;   // score-table candidates per chunk
+  off = align_up(off + sa::tables_stage_bytes(p));
   l.total = off;
   return l;
 }
@@ -403,6 +409,7 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const f
   A.lens = seq_lens;
   A.cand = cand_idx;
   A.cand_cnt = cand_cnt;
+  sa::tables_stage_ptrs(p, at<void>(ws, l.stage), &A.stage, &A.stage_cnt);
   A.status = at<int>(ws, l.header);
   A.decay = decay;
   A.beta = beta;

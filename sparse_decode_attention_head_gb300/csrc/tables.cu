@@ -13,20 +13,24 @@
 // previous step (z, lse from sa_sparse_decode), 0 otherwise;
 // T_new = fma(r, T_old, w).  Candidate test: T_new > beta / |I| in fp32.
 //
-// One CTA per (sequence, query head) walks the positions in chunks of
-// kChunk: it builds the chunk's weights in shared memory (dense-set entries
-// directly, selected tokens from the sorted previous selection list), updates
-// and writes both tables (the slash entry tested at position i is offset
-// L - 1 - i), marks seeds, expands them, and appends the chunk's candidates
-// with a block-wide scan, so the list comes out ascending.  Tables are
-// double-buffered (read in, write out) so no CTA reads an entry another has
-// already rewritten.
+// One CTA per (chunk of kChunk positions, query head, sequence): it builds
+// the chunk's weights in shared memory (dense-set entries directly, selected
+// tokens from the sorted previous selection list), updates and writes both
+// tables (the slash entry tested at position i is offset L - 1 - i), marks
+// seeds (recomputing the 3-position halo its neighbours own), expands them,
+// and compacts the chunk's candidates in ascending order into a staging row
+// (at most min(kChunk, kcap) kept) with their count.  A second kernel
+// concatenates each head's chunks in order into the candidate list.  Tables
+// are double-buffered (read in, write out) so no CTA reads an entry another
+// has already rewritten.
+#include <algorithm>
+
 #include "sa_common.cuh"
 
 namespace sa {
 
-constexpr int kTabThreads = 1024;
-constexpr int kPer = 4;                        // positions per thread per chunk
+constexpr int kTabThreads = 512;
+constexpr int kPer = 8;                        // positions per thread per chunk
 constexpr int kChunk = kTabThreads * kPer;     // 4096
 constexpr int kHalo = 3;                       // seeds at i-2 .. i+1 expand onto i
 
@@ -43,44 +47,17 @@ struct TableArgs {
   const int* lens;
   int* cand;
   int* cand_cnt;
+  int* stage;      // [B * Hq][nchunks][min(kChunk, kcap)] candidates of each chunk
+  int* stage_cnt;  // [B * Hq][nchunks]
   int* status;
   float decay;
   float beta;
 };
 
-// First index in sorted list[0, n) with list[idx] >= x.
-__device__ __forceinline__ int lower_bound(const int* list, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(list + mid) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
-// Fill w[k] = weight of position base + k (k in [0, n)) for the previous step.
-__device__ void fill_weights(float* w, int base, int n, const TableArgs& A, const float* logits, int Lp,
-                             int ps_end, int pw_beg, const int* sel, int scnt, float lse, float one_minus_r) {
-  for (int k = threadIdx.x; k < n; k += blockDim.x) {
-    const int pos = base + k;
-    float x = 0.f;
-    if (pos >= 0 && pos < Lp && (pos < ps_end || pos >= pw_beg))
-      x = __fmul_rn(one_minus_r, expf(__ldg(logits + pos) - lse));
-    w[k] = x;
-  }
-  __syncthreads();
-  // selected tokens inside the previous middle region (the list is ascending)
-  __shared__ int s_range[2];
-  if (threadIdx.x == 0) {
-    s_range[0] = lower_bound(sel, scnt, max(base, ps_end));
-    s_range[1] = lower_bound(sel, scnt, min(base + n, pw_beg));
-  }
-  __syncthreads();
-  for (int e = s_range[0] + threadIdx.x; e < s_range[1]; e += blockDim.x) {
-    const int pos = __ldg(sel + e);
-    w[pos - base] = __fmul_rn(one_minus_r, expf(__ldg(logits + pos) - lse));
-  }
-  __syncthreads();
+// Weight fed to the tables by an entry the previous step attended:
+// (1 - r) e^(z - lse), z its logit.
+__device__ __forceinline__ float attended_weight(const float* logits, int pos, float lse, float one_minus_r) {
+  return __fmul_rn(one_minus_r, expf(__ldg(logits + pos) - lse));
 }
 
 __global__ void __launch_bounds__(kTabThreads)
@@ -93,7 +70,7 @@ tables_kernel(Params p, TableArgs A) {
   __shared__ int s_scan[32];
   __shared__ int s_total;
 
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.mpp * kP;                                  // table length
   const size_t row = ((size_t)b * p.Hq + h) * N;
@@ -121,105 +98,206 @@ tables_kernel(Params p, TableArgs A) {
     logits = A.prev_logits + row;
   }
   const int delta = L - Lp;   // positions the context grew by since the previous step
-  int* cand = A.cand + ((size_t)b * p.Hq + h) * p.kcap;
-  int found = 0;
+  const int nch = (N + kChunk - 1) / kChunk;
+  const int cap = min(kChunk, p.kcap);
+  const int row_id = b * p.Hq + h;
+  int* stage = A.stage + ((size_t)row_id * nch + blockIdx.x) * cap;
+  const int c0 = blockIdx.x * kChunk;
+  const int c1 = min(N, c0 + kChunk);
+  const int n = c1 - c0 + kHalo;                             // positions c0-2 .. c1
+  const int base_v = c0 - 2, base_s = c0 - 2 - delta;       // previous-step position of entry k
 
-  for (int c0 = 0; c0 < N; c0 += kChunk) {
-    const int c1 = min(N, c0 + kChunk);
-    const int n = c1 - c0 + kHalo;                           // positions c0-2 .. c1
+  // 1. this thread's entries, positions c0 + tid + q kTabThreads (so a warp's
+  //    loads are contiguous in both tables), loaded first
+  float vv[kPer], sv[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int j = c0 + tid + q * kTabThreads;
+    const int d = L - 1 - j;                                 // slash offset tested at this position
+    vv[q] = j < c1 ? __ldg(vin + j) : 0.f;
+    sv[q] = (j < c1 && d >= 0 && d < N) ? __ldg(sin + d) : 0.f;
+  }
+
+  // 2. the previous step's weights on the chunk (and its halo), in shared memory
+  if (has_prev) {
+    for (int k = tid; k < n; k += kTabThreads) {
+      s_wv[k] = 0.f;
+      s_ws[k] = 0.f;
+    }
+    __syncthreads();
+    // dense-set entries: [0, ps_end) and [pw_beg, Lp)
+    auto dense_fill = [&](float* w, int base) {
+      for (int pos = max(base, 0) + tid; pos < min(base + n, ps_end); pos += kTabThreads)
+        w[pos - base] = attended_weight(logits, pos, lse, one_minus_r);
+      for (int pos = max(base, pw_beg) + tid; pos < min(base + n, Lp); pos += kTabThreads)
+        w[pos - base] = attended_weight(logits, pos, lse, one_minus_r);
+    };
+    dense_fill(s_wv, base_v);
+    dense_fill(s_ws, base_s);
+    // selected entries inside the previous middle region: every thread scans
+    // part of the list (duplicates write the same value)
+    for (int e = tid; e < scnt; e += kTabThreads) {
+      const int pos = __ldg(sel + e);
+      if (pos < ps_end || pos >= pw_beg) continue;
+      const int kv = pos - base_v, ks = pos - base_s;
+      const bool inv = kv >= 0 && kv < n, ins = ks >= 0 && ks < n;
+      if (!inv && !ins) continue;
+      const float wt = attended_weight(logits, pos, lse, one_minus_r);
+      if (inv) s_wv[kv] = wt;
+      if (ins) s_ws[ks] = wt;
+    }
+    __syncthreads();
+  }
+
+  // 3. update, write the owned entries, mark seeds
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int j = c0 + tid + q * kTabThreads;
+    const int k = j - base_v;
+    if (j < c1) {
+      const float v = has_prev ? __fmaf_rn(r, vv[q], s_wv[k]) : vv[q];
+      const int d = L - 1 - j;
+      float s = 0.f;
+      if (d >= 0 && d < N) {
+        s = has_prev ? __fmaf_rn(r, sv[q], s_ws[k]) : sv[q];
+        sout[d] = s;
+      }
+      vout[j] = v;
+      s_seed[k] = j >= s_end && j < w_beg && (v > tau || s > tau);
+    }
+  }
+  if (tid < kHalo) {   // seeds of the halo: positions c0-2, c0-1 and c1, owned by the neighbours
+    const int j = tid < 2 ? c0 - 2 + tid : c1;
+    const int k = j - base_v;
+    bool seed = false;
+    if (j >= 0 && j < N && j >= s_end && j < w_beg) {
+      const float v = has_prev ? __fmaf_rn(r, __ldg(vin + j), s_wv[k]) : __ldg(vin + j);
+      const int d = L - 1 - j;
+      float s = 0.f;
+      if (d >= 0 && d < N) s = has_prev ? __fmaf_rn(r, __ldg(sin + d), s_ws[k]) : __ldg(sin + d);
+      seed = v > tau || s > tau;
+    }
+    s_seed[k] = seed;
+  }
+  // slash entries of negative positions (offset >= L) owned by this chunk
+  for (int d = max(c0, L) + tid; d < c1; d += kTabThreads) {
+    float s = __ldg(sin + d);
     if (has_prev) {
-      fill_weights(s_wv, c0 - 2, n, A, logits, Lp, ps_end, pw_beg, sel, scnt, lse, one_minus_r);
-      fill_weights(s_ws, c0 - 2 - delta, n, A, logits, Lp, ps_end, pw_beg, sel, scnt, lse, one_minus_r);
-    }
-    // update, write owned entries, mark seeds
-    for (int k = tid; k < n; k += blockDim.x) {
-      const int j = c0 - 2 + k;                              // position
-      bool seed = false;
-      if (j >= 0 && j < N) {
-        const float v = has_prev ? __fmaf_rn(r, __ldg(vin + j), s_wv[k]) : __ldg(vin + j);
-        const int d = L - 1 - j;                             // slash offset of position j
-        float s = 0.f;
-        if (d >= 0 && d < N) s = has_prev ? __fmaf_rn(r, __ldg(sin + d), s_ws[k]) : __ldg(sin + d);
-        if (j >= c0 && j < c1) {                             // owned: write
-          vout[j] = v;
-          if (d >= 0 && d < N) sout[d] = s;
-        }
-        seed = j >= s_end && j < w_beg && (v > tau || s > tau);
-      }
-      s_seed[k] = seed;
-    }
-    // slash entries of negative positions (offset >= L) owned by this chunk
-    for (int d = max(c0, L) + tid; d < c1; d += blockDim.x) {
-      float s = __ldg(sin + d);
-      if (has_prev) {
-        const int pos = Lp - 1 - d;                          // >= 0 only if the context shrank
-        float w = 0.f;
-        if (pos >= 0) {
-          bool att = pos < ps_end || pos >= pw_beg;
-          if (!att) {
-            const int e = lower_bound(sel, scnt, pos);
-            att = e < scnt && __ldg(sel + e) == pos;
+      const int pos = Lp - 1 - d;                            // >= 0 only if the context shrank
+      float w = 0.f;
+      if (pos >= 0) {
+        bool att = pos < ps_end || pos >= pw_beg;
+        if (!att) {
+          int lo = 0, hi = scnt;                             // first list entry >= pos
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(sel + mid) < pos) lo = mid + 1; else hi = mid;
           }
-          if (att) w = __fmul_rn(one_minus_r, expf(__ldg(logits + pos) - lse));
+          att = lo < scnt && __ldg(sel + lo) == pos;
         }
-        s = __fmaf_rn(r, s, w);
+        if (att) w = attended_weight(logits, pos, lse, one_minus_r);
       }
-      sout[d] = s;
+      s = __fmaf_rn(r, s, w);
     }
+    sout[d] = s;
+  }
+  __syncthreads();
+
+  // 4. expand: position i is a candidate if a seed sits at i-2, i-1, i or i+1
+  //    (thread tid takes the consecutive positions jb .., so the compaction
+  //    below keeps them ascending)
+  const int jb = c0 + kPer * tid;
+  int mine = 0;
+  bool is_c[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int i = jb + q;
+    const int k = i - base_v;
+    bool cnd = false;
+    if (i < c1 && i >= s_end && i < w_beg)
+      cnd = s_seed[k - 2] | s_seed[k - 1] | s_seed[k] | s_seed[k + 1];
+    is_c[q] = cnd;
+    mine += cnd;
+  }
+  // block exclusive scan of the per-thread counts (ascending positions)
+  const int x = warp_incl_scan(mine);
+  if (lane == 31) s_scan[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_incl_scan(lane < kTabThreads / 32 ? s_scan[lane] : 0);
+    if (lane < kTabThreads / 32) s_scan[lane] = w;
+    if (lane == kTabThreads / 32 - 1) s_total = w;
+  }
+  __syncthreads();
+  int pos = (warp > 0 ? s_scan[warp - 1] : 0) + x - mine;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    if (is_c[q]) {
+      if (pos < cap) stage[pos] = jb + q;
+      ++pos;
+    }
+  }
+  if (tid == 0) A.stage_cnt[(size_t)row_id * nch + blockIdx.x] = s_total;
+}
+
+// One CTA per (query head, sequence): the chunks' candidates, in chunk
+// order, form the ascending candidate list (kcap kept; more is
+// SA_ERR_CAPACITY).
+__global__ void __launch_bounds__(256)
+tables_compact_kernel(Params p, TableArgs A) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_off[2];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int N = p.mpp * kP;
+  const int nch = (N + kChunk - 1) / kChunk;
+  const int cap = min(kChunk, p.kcap);
+  const int row_id = b * p.Hq + h;
+  const int* cnt = A.stage_cnt + (size_t)row_id * nch;
+  int* cand = A.cand + (size_t)row_id * p.kcap;
+  if (tid == 0) s_off[0] = 0;
+  __syncthreads();
+  for (int c = 0; c < nch; ++c) {
+    const int off = s_off[0];
+    const int n = cnt[c];
+    const int* st = A.stage + ((size_t)row_id * nch + c) * cap;
+    for (int e = tid; e < min(n, cap); e += blockDim.x)
+      if (off + e < p.kcap) cand[off + e] = st[e];
     __syncthreads();
-    // expand: position i is a candidate if a seed sits at i-2, i-1, i or i+1
-    int mine = 0;
-    bool is_c[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int i = c0 + tid * kPer + q;
-      const int k = i - (c0 - 2);
-      bool cnd = false;
-      if (i < c1 && i >= s_end && i < w_beg)
-        cnd = s_seed[k - 2] | s_seed[k - 1] | s_seed[k] | s_seed[k + 1];
-      is_c[q] = cnd;
-      mine += cnd;
-    }
-    // block exclusive scan of the per-thread counts (ascending positions)
-    int x = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_scan[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int w = s_scan[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      s_scan[lane] = w;
-      if (lane == 31) s_total = w;
-    }
-    __syncthreads();
-    int pos = found + (warp > 0 ? s_scan[warp - 1] : 0) + x - mine;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      if (is_c[q]) {
-        if (pos < p.kcap) cand[pos] = c0 + tid * kPer + q;
-        ++pos;
-      }
-    }
-    found += s_total;
+    if (tid == 0) s_off[0] = off + n;
     __syncthreads();
   }
   if (tid == 0) {
-    A.cand_cnt[(size_t)b * p.Hq + h] = min(found, p.kcap);
+    const int found = s_off[0];
+    A.cand_cnt[row_id] = min(found, p.kcap);
     if (found > p.kcap) set_status(A.status, SA_ERR_CAPACITY);
   }
 }
 
+
+
+size_t tables_stage_bytes(const Params& p) {
+  const size_t N = (size_t)p.mpp * kP;
+  const size_t nch = (N + kChunk - 1) / kChunk;
+  const size_t cap = std::min<size_t>(kChunk, (size_t)std::max(p.kcap, 1));
+  return (size_t)p.B * p.Hq * nch * (cap + 1) * sizeof(int);
+}
+
+// The staging area at `base` (tables_stage_bytes): candidates, then counts.
+void tables_stage_ptrs(const Params& p, void* base, int** stage, int** cnt) {
+  const size_t N = (size_t)p.mpp * kP;
+  const size_t nch = (N + kChunk - 1) / kChunk;
+  const size_t cap = std::min<size_t>(kChunk, (size_t)std::max(p.kcap, 1));
+  *stage = static_cast<int*>(base);
+  *cnt = *stage + (size_t)p.B * p.Hq * nch * cap;
+}
+
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream) {
-  dim3 grid(p.Hq, p.B);
-  const cudaError_t e = launch_pdl(tables_kernel, grid, dim3(kTabThreads), 0, stream, p, A);
+  const int N = p.mpp * kP;
+  const int nch = (N + kChunk - 1) / kChunk;
+  cudaError_t e = launch_pdl(tables_kernel, dim3(nch, p.Hq, p.B), dim3(kTabThreads), 0, stream, p, A);
+  if (e != cudaSuccess) return SA_ERR_CUDA;
+  e = launch_pdl(tables_compact_kernel, dim3(p.Hq, p.B), dim3(256), 0, stream, p, A);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
