@@ -66,7 +66,10 @@ tables_kernel(Params p, TableArgs A) {
   pdl_trigger();
   __shared__ float s_wv[kChunk + kHalo];       // weights feeding the vertical entries (positions c0-2 ..)
   __shared__ float s_ws[kChunk + kHalo];       // weights feeding the slash entries tested there
-  __shared__ unsigned char s_seed[kChunk + kHalo];
+  // seed bits by position offset o = j - c0, stored at bit o + 32: word 0
+  // holds the left halo (o = -2, -1 at bits 30, 31), words 1 .. kChunk / 32
+  // the chunk, the word after them the right halo (o = kChunk)
+  __shared__ uint32_t s_seed[kChunk / 32 + 2];
   __shared__ int s_scan[32];
   __shared__ int s_total;
 
@@ -149,11 +152,15 @@ tables_kernel(Params p, TableArgs A) {
     __syncthreads();
   }
 
-  // 3. update, write the owned entries, mark seeds
+  // 3. update, write the owned entries, mark seeds (a warp's 32 positions are
+  //    consecutive, so one ballot gives one word of seed bits)
+  if (tid == 0) s_seed[0] = 0u;
+  if (tid == 1) s_seed[kChunk / 32 + 1] = 0u;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int j = c0 + tid + q * kTabThreads;
     const int k = j - base_v;
+    bool seed = false;
     if (j < c1) {
       const float v = has_prev ? __fmaf_rn(r, vv[q], s_wv[k]) : vv[q];
       const int d = L - 1 - j;
@@ -163,9 +170,12 @@ tables_kernel(Params p, TableArgs A) {
         sout[d] = s;
       }
       vout[j] = v;
-      s_seed[k] = j >= s_end && j < w_beg && (v > tau || s > tau);
+      seed = j >= s_end && j < w_beg && (v > tau || s > tau);
     }
+    const uint32_t word = __ballot_sync(0xffffffffu, seed);
+    if (lane == 0) s_seed[1 + (tid + q * kTabThreads) / 32] = word;
   }
+  __syncthreads();
   if (tid < kHalo) {   // seeds of the halo: positions c0-2, c0-1 and c1, owned by the neighbours
     const int j = tid < 2 ? c0 - 2 + tid : c1;
     const int k = j - base_v;
@@ -177,7 +187,10 @@ tables_kernel(Params p, TableArgs A) {
       if (d >= 0 && d < N) s = has_prev ? __fmaf_rn(r, __ldg(sin + d), s_ws[k]) : __ldg(sin + d);
       seed = v > tau || s > tau;
     }
-    s_seed[k] = seed;
+    if (seed) {
+      const int bit = j - c0 + 32;
+      atomicOr(&s_seed[bit >> 5], 1u << (bit & 31));
+    }
   }
   // slash entries of negative positions (offset >= L) owned by this chunk
   for (int d = max(c0, L) + tid; d < c1; d += kTabThreads) {
@@ -207,18 +220,18 @@ tables_kernel(Params p, TableArgs A) {
   //    (thread tid takes the consecutive positions jb .., so the compaction
   //    below keeps them ascending)
   const int jb = c0 + kPer * tid;
-  int mine = 0;
-  bool is_c[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int i = jb + q;
-    const int k = i - base_v;
-    bool cnd = false;
-    if (i < c1 && i >= s_end && i < w_beg)
-      cnd = s_seed[k - 2] | s_seed[k - 1] | s_seed[k] | s_seed[k + 1];
-    is_c[q] = cnd;
-    mine += cnd;
+  uint32_t cbits;
+  {
+    // bits of positions jb - 2 .. jb + 9 start at bit 8 tid + 30
+    const int b0 = kPer * tid + 30;
+    const uint64_t w = ((uint64_t)s_seed[(b0 >> 5) + 1] << 32) | s_seed[b0 >> 5];
+    const uint32_t win = (uint32_t)(w >> (b0 & 31));          // bit x: position jb - 2 + x
+    cbits = (win | (win >> 1) | (win >> 2) | (win >> 3)) & 0xffu;
+    // positions outside the middle region or the chunk are no candidates
+    const int lo = max(s_end, jb), hi = min(min(w_beg, c1), jb + kPer);
+    cbits = hi > lo ? cbits & (((1u << (hi - lo)) - 1u) << (lo - jb)) : 0u;
   }
+  const int mine = __popc(cbits);
   // block exclusive scan of the per-thread counts (ascending positions)
   const int x = warp_incl_scan(mine);
   if (lane == 31) s_scan[warp] = x;
@@ -232,7 +245,7 @@ tables_kernel(Params p, TableArgs A) {
   int pos = (warp > 0 ? s_scan[warp - 1] : 0) + x - mine;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    if (is_c[q]) {
+    if ((cbits >> q) & 1u) {
       if (pos < cap) stage[pos] = jb + q;
       ++pos;
     }
@@ -242,39 +255,49 @@ tables_kernel(Params p, TableArgs A) {
 
 // One CTA per (query head, sequence): the chunks' candidates, in chunk
 // order, form the ascending candidate list (kcap kept; more is
-// SA_ERR_CAPACITY).
+// SA_ERR_CAPACITY).  The chunk counts are scanned 256 at a time; each warp
+// copies whole chunks.
 __global__ void __launch_bounds__(256)
 tables_compact_kernel(Params p, TableArgs A) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int s_off[2];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  __shared__ int s_off[256];
+  __shared__ int s_w[8];
+  __shared__ int s_carry;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.mpp * kP;
   const int nch = (N + kChunk - 1) / kChunk;
   const int cap = min(kChunk, p.kcap);
   const int row_id = b * p.Hq + h;
   const int* cnt = A.stage_cnt + (size_t)row_id * nch;
   int* cand = A.cand + (size_t)row_id * p.kcap;
-  if (tid == 0) s_off[0] = 0;
-  __syncthreads();
-  for (int c = 0; c < nch; ++c) {
-    const int off = s_off[0];
-    const int n = cnt[c];
-    const int* st = A.stage + ((size_t)row_id * nch + c) * cap;
-    for (int e = tid; e < min(n, cap); e += blockDim.x)
-      if (off + e < p.kcap) cand[off + e] = st[e];
+  if (tid == 0) s_carry = 0;
+  for (int c0 = 0; c0 < nch; c0 += 256) {
+    const int c = c0 + tid;
+    const int n = c < nch ? cnt[c] : 0;
+    const int x = warp_incl_scan(n);
+    if (lane == 31) s_w[warp] = x;
     __syncthreads();
-    if (tid == 0) s_off[0] = off + n;
+    int before = s_carry + x - n;
+    for (int w = 0; w < warp; ++w) before += s_w[w];
+    s_off[tid] = before;
+    __syncthreads();
+    for (int cc = warp; cc < min(256, nch - c0); cc += 8) {
+      const int off = s_off[cc];
+      const int m = min(cnt[c0 + cc], cap);
+      const int* st = A.stage + ((size_t)row_id * nch + c0 + cc) * cap;
+      for (int e = lane; e < m && off + e < p.kcap; e += 32) cand[off + e] = st[e];
+    }
+    __syncthreads();
+    if (tid == 255) s_carry = before + n;
     __syncthreads();
   }
   if (tid == 0) {
-    const int found = s_off[0];
+    const int found = s_carry;
     A.cand_cnt[row_id] = min(found, p.kcap);
     if (found > p.kcap) set_status(A.status, SA_ERR_CAPACITY);
   }
 }
-
-
 
 size_t tables_stage_bytes(const Params& p) {
   const size_t N = (size_t)p.mpp * kP;
