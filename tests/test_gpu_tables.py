@@ -102,3 +102,67 @@ def test_tables_128k_llama_shape_64_steps():
     heads = [(0, 0), (1, 9), (2, 17), (3, 31)]
     n = _run(wl, 3, wl.steps, heads=heads)
     assert min(n) > 0
+
+
+def test_tables_small_free_running_overlap():
+    """Free-running comparison (reported, not gated): the GPU path and the
+    oracle each carry their own tables over all steps, and the candidate sets
+    they pick are compared per step by Jaccard overlap.  exp() differs in the
+    last bits between the two, so a weight near the threshold can flip a
+    candidate and the runs drift apart; the teacher-forced tests above are the
+    parity gate."""
+    wl = synth.table_workload("tables_small")
+    case = synth.make_table_case(wl, 5)
+    B, Hq, Hk, G = wl.B, wl.Hq, wl.Hk, wl.G
+    mpp = wl.max_pages_per_seq
+    N = mpp * wl.P
+    prob = sa.Problem(B=B, Hq=Hq, Hk=Hk, max_pages_per_seq=mpp, num_pages=B * mpp, sink=wl.S, window=wl.W,
+                      block_sizes=[16] * Hk, k_per_head=[0] * Hq, kcap=wl.kcap)
+    ws = sa.Workspace(prob)
+    kp, vp, pt = case.k_pool.cuda(), case.v_pool.cuda(), case.page_table.cuda()
+    kp_np, vp_np, pt_np = orc.to_np(case.k_pool), orc.to_np(case.v_pool), orc.to_np(case.page_table)
+    tv = [case.vert0.cuda(), torch.empty(B, Hq, N, device="cuda")]
+    ts = [case.slash0.cuda(), torch.empty(B, Hq, N, device="cuda")]
+    cand = [torch.zeros(B, Hq, wl.kcap, dtype=torch.int32, device="cuda") for _ in range(2)]
+    cnt = [torch.zeros(B, Hq, dtype=torch.int32, device="cuda") for _ in range(2)]
+    logits = torch.zeros(B, Hq, N, device="cuda")
+    ov = orc.to_np(case.vert0).astype(np.float64)
+    osl = orc.to_np(case.slash0).astype(np.float64)
+    prev = None
+    o_prev = None
+    jaccard = []
+    for t in range(wl.steps):
+        L = wl.L0 + t
+        seq_lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        cur, nxt = t % 2, (t + 1) % 2
+        sa.update_score_tables(prob, tv[cur], ts[cur], tv[nxt], ts[nxt], seq_lens, cand[cur], cnt[cur], ws,
+                               beta=wl.beta, prev=prev)
+        q = case.q_steps[t].cuda()
+        dev = dict(q=q, k_pool=kp, v_pool=vp, page_table=pt, seq_lens=seq_lens)
+        o, l = H.gpu_decode(prob, dev, cand[cur], cnt[cur], ws, gran=sa.SEL_TOKEN, logits=logits)
+        torch.cuda.synchronize()
+        assert ws.status() == sa.SA_OK
+        c_gpu, n_gpu = cand[cur].cpu().numpy(), cnt[cur].cpu().numpy()
+        step = []
+        new_o = {}
+        for b in range(B):
+            for h in range(Hq):
+                kseq = orc.gather_sequence(kp_np, pt_np[b], h // G, L)
+                if o_prev is not None:   # the oracle's own update from its own previous step
+                    qp, Lp, cp = o_prev[(b, h)]
+                    pos, w = orc.merged_weights(qp, orc.gather_sequence(kp_np, pt_np[b], h // G, Lp), Lp, wl.S,
+                                                wl.W, cp, prob.scale)
+                    ov[b, h], osl[b, h] = orc.table_update(ov[b, h], osl[b, h], Lp, pos, w)
+                c_ref, _ = orc.table_candidates(ov[b, h].astype(np.float32), osl[b, h].astype(np.float32), L,
+                                                wl.S, wl.W, wl.beta, wl.kcap)
+                a = set(c_gpu[b, h, :n_gpu[b, h]].tolist())
+                r = set(c_ref.tolist())
+                step.append(len(a & r) / max(1, len(a | r)))
+                new_o[(b, h)] = (orc.to_np(case.q_steps[t, b, h]), L, c_ref)
+        o_prev = new_o
+        jaccard.append(float(np.mean(step)))
+        prev = dict(prev_seq_lens=seq_lens, prev_sel_idx=cand[cur], prev_sel_cnt=cnt[cur], prev_logits=logits,
+                    prev_lse=l)
+    print("free-running Jaccard per step:", " ".join(f"{x:.3f}" for x in jaccard))
+    assert len(jaccard) == wl.steps and all(0.0 <= x <= 1.0 for x in jaccard)
+    assert jaccard[0] == 1.0   # step 0 starts from the same tables
