@@ -49,6 +49,10 @@ Readings where the pages are silent (each also listed in the design notes):
       slash by offset (L - 1 - i); one threshold tau = beta / |I|, strict
       comparison; expansion {-1, 0, 1, 2} clipped to M; at most kcap tokens
       (lowest positions kept).
+  R9  Group-shared selection (a variant; the pages select per head): the
+      blocks of a KV head are ranked by the fp32 sum, in head order, of its G
+      query heads' canonical scores; every head of the group keeps the same k
+      blocks (ties by lower block index).
 """
 from __future__ import annotations
 
@@ -367,3 +371,31 @@ def table_candidates(vert32, slash32, L: int, S: int, W: int, beta: float, kcap:
                 cand.add(j)
     out = np.array(sorted(cand), dtype=np.int64)
     return out[:kcap], len(out) > kcap
+
+
+# ---------------------------------------------------------------------------
+# variant: one selection shared by the query heads of a KV group (reading R9)
+# ---------------------------------------------------------------------------
+
+def group_scores(per_head_scores) -> np.ndarray:
+    """Fp32 sum of the group's canonical block scores in head order, one
+    rounding per addition (reading R9)."""
+    acc = np.asarray(per_head_scores[0], dtype=F32).copy()
+    for sc in per_head_scores[1:]:
+        acc = (acc + np.asarray(sc, dtype=F32)).astype(F32)
+    return acc
+
+
+def select_group(q32_group, kseq, L, S, W, Bs, k, mode):
+    """One block selection for all query heads of a KV head (reading R9):
+    summaries -> each head's canonical scores -> their fp32 sum -> top-k.
+    Returns (selected block ids ascending, candidate ids, group scores)."""
+    j0, j1 = candidate_blocks(L, S, W, Bs)
+    ids = np.arange(j0, j1, dtype=np.int64)
+    if j1 <= j0:
+        return np.zeros(0, dtype=np.int64), ids, np.zeros(0, dtype=F32)
+    if k >= j1 - j0:
+        return ids.copy(), ids, None
+    summ = summarize_sequence(kseq, Bs, mode, j0, j1)
+    sc = group_scores([score_blocks(q, summ, mode) for q in q32_group])
+    return topk_blocks(sc, ids, k), ids, sc

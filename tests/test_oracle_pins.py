@@ -332,3 +332,59 @@ def test_empty_sequence():
     K = np.zeros((0, 128), F32)
     r = orc.decode_head(q, K, K, 0, 4, 64, 16, [], 0.1)
     assert np.all(r["O"] == 0) and r["lse"] == -math.inf
+
+
+# ---------------------------------------------------------------------------
+# variant: group-shared selection (reading R9)
+# ---------------------------------------------------------------------------
+
+def _group_case(seed, G, n_blocks, Bs=16, D=128):
+    rng = np.random.default_rng(seed)
+    L = n_blocks * Bs
+    kseq = orc.bf16_rne(rng.standard_normal((L, D)).astype(np.float32))
+    qs = [orc.bf16_rne(rng.standard_normal(D).astype(np.float32)) for _ in range(G)]
+    return qs, kseq, L
+
+
+def test_group_selection_of_one_head_is_the_head_selection():
+    qs, kseq, L = _group_case(1, 1, 40)
+    for mode in (orc.SUMMARY_MINMAX, orc.SUMMARY_MEAN):
+        for k in (0, 1, 5, 17, 39):
+            a, _, _ = orc.select_head(qs[0], kseq, L, 0, 16, 16, k, mode)
+            b, _, _ = orc.select_group(qs, kseq, L, 0, 16, 16, k, mode)
+            assert np.array_equal(a, b)
+
+
+def test_group_selection_maximises_the_group_score_sum():
+    # brute force over every k-subset of a small candidate range: the chosen
+    # blocks carry the largest total group score (exact fp64 sums of the fp32
+    # group scores; with distinct scores the optimum is unique)
+    import itertools
+    for seed in range(4):
+        qs, kseq, L = _group_case(10 + seed, 3, 12)
+        for k in (1, 2, 4, 6):
+            sel, ids, sc = orc.select_group(qs, kseq, L, 0, 16, 16, k, orc.SUMMARY_MINMAX)
+            assert len(np.unique(sc)) == len(sc)
+            best = max(itertools.combinations(range(len(ids)), k), key=lambda c: sum(float(sc[i]) for i in c))
+            assert np.array_equal(sel, np.sort(ids[list(best)]))
+
+
+def test_group_sum_can_overrule_a_single_head():
+    # a block one head likes strongly but the other three dislike is kept by
+    # that head alone, and dropped by the group when the others' dislike wins
+    D, Bs, n = 128, 16, 20
+    rng = np.random.default_rng(7)
+    base = rng.standard_normal((n * Bs, D)).astype(np.float32) * 0.05
+    u = np.zeros(D, np.float32); u[0] = 1.0
+    w = np.zeros(D, np.float32); w[1] = 1.0
+    kseq = base.copy()
+    kseq[5 * Bs:6 * Bs] += 4.0 * u          # block 5: along u
+    kseq[9 * Bs:10 * Bs] += 1.0 * w         # block 9: mildly along w
+    kseq = orc.bf16_rne(kseq)
+    q_like = orc.bf16_rne((8.0 * u + 0.5 * w).astype(np.float32))
+    q_dis = orc.bf16_rne((-8.0 * u + 2.0 * w).astype(np.float32))
+    qs = [q_like, q_dis, q_dis, q_dis]
+    own, _, _ = orc.select_head(q_like, kseq, n * Bs, 0, 16, Bs, 1, orc.SUMMARY_MEAN)
+    grp, _, sc = orc.select_group(qs, kseq, n * Bs, 0, 16, Bs, 1, orc.SUMMARY_MEAN)
+    assert own.tolist() == [5]
+    assert grp.tolist() == [9]
