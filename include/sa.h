@@ -75,6 +75,12 @@ extern "C" {
 #define SA_SUMMARY_MINMAX 0 /* [..][2][D]: row 0 = per-dim min, row 1 = per-dim max */
 #define SA_SUMMARY_MEAN 1   /* [..][D]: bf16(RNE(fp32 ascending sum / n)) */
 
+/* how blocks are selected (sa_problem.selection_mode) */
+#define SA_SELECT_PER_HEAD 0 /* each query head keeps its own top-k blocks */
+#define SA_SELECT_GROUP 1    /* the G query heads of a KV head share one top-k, ranked by the fp32 sum
+                                of their scores in head order; every head of a group must have the
+                                same k.  A variant: the pages select per head. */
+
 /* granularity of a selection list handed to sa_sparse_decode */
 #define SA_SEL_BLOCK 0 /* entries are block indices of the head's KV head */
 #define SA_SEL_TOKEN 1 /* entries are token positions */
@@ -106,6 +112,7 @@ typedef struct sa_problem {
   const int32_t* k_per_qhead;        /* host [Hq], blocks kept per head, 0 <= k <= kcap */
   int32_t kcap;                /* capacity of a selection list (entries per head) */
   float scale;                 /* softmax scale, normally 1/sqrt(D) */
+  int32_t selection_mode;      /* SA_SELECT_PER_HEAD (0, the pages' selection) or SA_SELECT_GROUP */
 } sa_problem;
 
 /* Block slots per (sequence, KV head) in the summary and score tensors:

@@ -80,6 +80,7 @@ int make_params(const sa_problem* pr, Params* p) {
   if (pr->summary_mode != SA_SUMMARY_MINMAX && pr->summary_mode != SA_SUMMARY_MEAN) return SA_ERR_INVALID_ARG;
   if (pr->block_size_per_kvh == nullptr || pr->k_per_qhead == nullptr) return SA_ERR_INVALID_ARG;
   if (pr->kcap < 1) return SA_ERR_INVALID_ARG;
+  if (pr->selection_mode != SA_SELECT_PER_HEAD && pr->selection_mode != SA_SELECT_GROUP) return SA_ERR_INVALID_ARG;
   if (!(pr->scale > 0.f) || !std::isfinite(pr->scale)) return SA_ERR_INVALID_ARG;
   if ((long long)pr->max_pages_per_seq * SA_PAGE_SIZE >= (1LL << 30)) return SA_ERR_UNSUPPORTED;
   if ((long long)pr->num_pages * pr->Hk * SA_PAGE_SIZE >= (1LL << 31)) return SA_ERR_UNSUPPORTED;
@@ -95,8 +96,12 @@ int make_params(const sa_problem* pr, Params* p) {
   for (int i = 0; i < pr->Hq; ++i) {
     if (pr->k_per_qhead[i] < 0) return SA_ERR_INVALID_ARG;
     if (pr->k_per_qhead[i] > pr->kcap) return SA_ERR_CAPACITY;
+    // a shared selection needs one budget per group
+    if (pr->selection_mode == SA_SELECT_GROUP && pr->k_per_qhead[i] != pr->k_per_qhead[i - i % (pr->Hq / pr->Hk)])
+      return SA_ERR_INVALID_ARG;
   }
   std::memset(p, 0, sizeof(*p));
+  p->sel_mode = pr->selection_mode;
   p->B = pr->B;
   p->Hq = pr->Hq;
   p->Hk = pr->Hk;

@@ -27,6 +27,7 @@ struct Params {
   int kcap;
   int slots;        // block slots per (b, kvh)
   float scale;
+  int sel_mode;     // SA_SELECT_*
   int bs[SA_MAX_HK];
   int k[SA_MAX_HQ];
 };

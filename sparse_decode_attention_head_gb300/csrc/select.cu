@@ -262,9 +262,24 @@ topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ 
   pdl_wait();
   pdl_trigger();
   __shared__ TopkScratch S;
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int b = blockIdx.y;
   const int L = min(seq_lens[b], p.mpp * kP);
   int j0, j1;
+  if (p.sel_mode == SA_SELECT_GROUP) {   // one CTA per KV head: the group's summed scores, one list for all
+    const int kvh = blockIdx.x, h0 = kvh * p.G;
+    candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
+    int* row0 = sel_idx + ((size_t)b * p.Hq + h0) * p.kcap;
+    group_topk<NT, KPT>(scores + ((size_t)b * p.Hq + h0) * p.slots + j0, j1 - j0, p.k[h0], j0, row0,
+                        sel_cnt + (size_t)b * p.Hq + h0, 0, S, p.G, (size_t)p.slots);
+    __syncthreads();
+    const int cnt = sel_cnt[(size_t)b * p.Hq + h0];
+    for (int g = 1; g < p.G; ++g) {
+      for (int i = threadIdx.x; i < cnt; i += NT) row0[(size_t)g * p.kcap + i] = row0[i];
+      if (threadIdx.x == 0) sel_cnt[(size_t)b * p.Hq + h0 + g] = cnt;
+    }
+    return;
+  }
+  const int h = blockIdx.x;
   candidate_range(L, p.S, p.W, p.bs[h / p.G], j0, j1);
   group_topk<NT, KPT>(scores + ((size_t)b * p.Hq + h) * p.slots + j0, j1 - j0, p.k[h], j0,
                       sel_idx + ((size_t)b * p.Hq + h) * p.kcap, sel_cnt + (size_t)b * p.Hq + h, 0, S);
@@ -315,7 +330,7 @@ size_t topk_smem_bytes(const Params&) { return 0; }
 
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream) {
-  dim3 grid(p.Hq, p.B);
+  dim3 grid(p.sel_mode == SA_SELECT_GROUP ? p.Hk : p.Hq, p.B);
   // the largest candidate count any head can have
   int max_n = 0;
   for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);

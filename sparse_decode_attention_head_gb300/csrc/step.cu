@@ -90,7 +90,14 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   int j0, j1;
   candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
   const int g = tid / GROUP;
-  if (g < G) {
+  if (p.sel_mode == SA_SELECT_GROUP) {   // one list for the group, from the summed scores
+    if (g == 0)
+      group_topk<GROUP, KPT>(scores + ((size_t)b * p.Hq + kvh * G) * p.slots + j0, j1 - j0, p.k[kvh * G], j0,
+                             s_sel, s_cnt, 1, S[0], G, (size_t)p.slots);
+    __syncthreads();
+    for (int i = tid; i < (G - 1) * p.kcap; i += kStepBuildThreads) s_sel[p.kcap + i] = s_sel[i % p.kcap];
+    if (tid > 0 && tid < G) s_cnt[tid] = s_cnt[0];
+  } else if (g < G) {
     const int h = kvh * G + g;
     group_topk<GROUP, KPT>(scores + ((size_t)b * p.Hq + h) * p.slots + j0, j1 - j0, p.k[h], j0,
                            s_sel + g * p.kcap, s_cnt + g, 1 + g, S[g]);

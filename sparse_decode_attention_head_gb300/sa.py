@@ -31,6 +31,8 @@ SUMMARY_MINMAX = 0
 SUMMARY_MEAN = 1
 SEL_BLOCK = 0
 SEL_TOKEN = 1
+SELECT_PER_HEAD = 0
+SELECT_GROUP = 1
 BLOCKS_TAIL = -1
 HEAD_DIM = 128
 PAGE_SIZE = 16
@@ -48,7 +50,7 @@ class _Problem(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
         ("sink", ctypes.c_int32), ("window", ctypes.c_int32), ("summary_mode", ctypes.c_int32),
         ("block_size_per_kvh", ctypes.POINTER(ctypes.c_int32)), ("k_per_qhead", ctypes.POINTER(ctypes.c_int32)),
-        ("kcap", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("kcap", ctypes.c_int32), ("scale", ctypes.c_float), ("selection_mode", ctypes.c_int32),
     ]
 
 
@@ -133,7 +135,7 @@ class Problem:
     def __init__(self, B: int, Hq: int, Hk: int, max_pages_per_seq: int, num_pages: int, sink: int,
                  window: int, block_sizes: Sequence[int], k_per_head: Sequence[int], kcap: int,
                  mode: int = SUMMARY_MINMAX, scale: Optional[float] = None, D: int = HEAD_DIM,
-                 page_size: int = PAGE_SIZE):
+                 page_size: int = PAGE_SIZE, selection: int = SELECT_PER_HEAD):
         self.B, self.Hq, self.Hk, self.D = B, Hq, Hk, D
         self.max_pages_per_seq, self.num_pages = max_pages_per_seq, num_pages
         self.sink, self.window, self.mode, self.kcap = sink, window, mode, kcap
@@ -146,7 +148,8 @@ class Problem:
         self._summary_shape = None
         self._c = _Problem(B, Hq, Hk, D, page_size, max_pages_per_seq, num_pages, sink, window, mode,
                            ctypes.cast(self._bs, ctypes.POINTER(ctypes.c_int32)),
-                           ctypes.cast(self._k, ctypes.POINTER(ctypes.c_int32)), kcap, self.scale)
+                           ctypes.cast(self._k, ctypes.POINTER(ctypes.c_int32)), kcap, self.scale, selection)
+        self.selection = selection
 
     @property
     def G(self):

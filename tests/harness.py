@@ -51,12 +51,13 @@ def to_np_case(case: synth.DecodeCase) -> NpCase:
 
 
 def make_problem(wl: synth.Workload, ks: Sequence[int], kcap: Optional[int] = None,
-                 mode: str = "minmax", num_pages: Optional[int] = None) -> sa.Problem:
+                 mode: str = "minmax", num_pages: Optional[int] = None,
+                 selection: int = sa.SELECT_PER_HEAD) -> sa.Problem:
     kc = max(1, max(ks)) if kcap is None else kcap
     npg = wl.B * wl.max_pages_per_seq if num_pages is None else num_pages
     return sa.Problem(B=wl.B, Hq=wl.Hq, Hk=wl.Hk, max_pages_per_seq=wl.max_pages_per_seq,
                       num_pages=npg, sink=wl.S, window=wl.W, block_sizes=wl.block_sizes,
-                      k_per_head=list(ks), kcap=kc, mode=MODES[mode])
+                      k_per_head=list(ks), kcap=kc, mode=MODES[mode], selection=selection)
 
 
 def to_dev(case: synth.DecodeCase, device="cuda"):
@@ -95,6 +96,23 @@ def oracle_select(nc: NpCase, wl: synth.Workload, ks: Sequence[int], mode: str,
                 continue
             sc = orc.score_blocks(nc.q[b, h], summ, mode)
             res[(b, h)] = (orc.topk_blocks(sc, ids, ks[h]), ids, sc)
+    return res
+
+
+def oracle_select_group(nc: NpCase, wl: synth.Workload, ks: Sequence[int], mode: str,
+                        units: Optional[List[Tuple[int, int]]] = None):
+    """Group-shared selection: {(b, h): (selected ascending, candidate ids,
+    group scores or None)}, the same entry for every head of a group."""
+    res = {}
+    units = units if units is not None else [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
+    for b, kvh in units:
+        kseq, _ = oracle_kv(nc, b, kvh)
+        L = int(nc.seq_lens[b])
+        Bs = wl.block_sizes[kvh]
+        q_group = [nc.q[b, kvh * wl.G + g] for g in range(wl.G)]
+        r = orc.select_group(q_group, kseq, L, wl.S, wl.W, Bs, ks[kvh * wl.G], mode)
+        for g in range(wl.G):
+            res[(b, kvh * wl.G + g)] = r
     return res
 
 

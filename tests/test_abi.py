@@ -88,3 +88,17 @@ def test_prepared_step_call_checks_its_tensors_once():
     cpu = torch.zeros(1, 4, 128, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         sa.DecodeStepCall(prob, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, None)
+
+
+def test_group_selection_needs_one_budget_per_group():
+    import ctypes
+    from sparse_decode_attention_head_gb300 import sa
+    ok = sa.Problem(B=1, Hq=8, Hk=2, max_pages_per_seq=16, num_pages=16, sink=4, window=64, block_sizes=[16, 16],
+                    k_per_head=[3] * 4 + [5] * 4, kcap=8, selection=sa.SELECT_GROUP)
+    assert sa.lib().sa_workspace_size(ok.ref) > 0
+    bad = sa.Problem(B=1, Hq=8, Hk=2, max_pages_per_seq=16, num_pages=16, sink=4, window=64, block_sizes=[16, 16],
+                     k_per_head=[3, 3, 3, 4, 5, 5, 5, 5], kcap=8, selection=sa.SELECT_GROUP)
+    assert sa.lib().sa_workspace_size(bad.ref) == 0
+    odd = sa.Problem(B=1, Hq=8, Hk=2, max_pages_per_seq=16, num_pages=16, sink=4, window=64, block_sizes=[16, 16],
+                     k_per_head=[3] * 8, kcap=8, selection=7)
+    assert sa.lib().sa_workspace_size(odd.ref) == 0
