@@ -169,7 +169,11 @@ int sa_score_blocks(const sa_problem* prob, const void* q,
  * keeps every candidate without scoring (a 100 % budget is dense attention).
  * sel_idx: [B][Hq][kcap] int32; sel_cnt: [B][Hq] int32.
  * scores_or_null: if not NULL, the scores are also written as in
- * sa_score_blocks.  Requires k_per_qhead[h] <= kcap (else SA_ERR_CAPACITY). */
+ * sa_score_blocks.  Requires k_per_qhead[h] <= kcap (else SA_ERR_CAPACITY).
+ * With prob->selection_mode == SA_SELECT_GROUP the ranking of a KV head's
+ * blocks is the fp32 sum of its G heads' scores, added in head order, and the
+ * G rows of sel_idx / sel_cnt receive the same list (a variant: Fluxion's
+ * core claim selects per head). */
 int sa_select_topk(const sa_problem* prob, const void* q,
                    const void* summaries, const int32_t* seq_lens,
                    int32_t* sel_idx, int32_t* sel_cnt, float* scores_or_null,
