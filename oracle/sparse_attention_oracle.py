@@ -49,6 +49,11 @@ Readings where the pages are silent (each also listed in the design notes):
       slash by offset (L - 1 - i); one threshold tau = beta / |I|, strict
       comparison; expansion {-1, 0, 1, 2} clipped to M; at most kcap tokens
       (lowest positions kept).
+  R10 Exact top-k inside the table candidates (LFPS, "The reading": an exact
+      top-k needs a dot product against every key; the tables only narrow the
+      keys down): each candidate token's score is the canonical fp32 dot
+      product of q with its bf16 key row (reading R4's order), and the k best
+      by (score descending, position ascending) are kept, reported ascending.
   R9  Group-shared selection (a variant; the pages select per head): the
       blocks of a KV head are ranked by the fp32 sum, in head order, of its G
       query heads' canonical scores; every head of the group keeps the same k
@@ -399,3 +404,19 @@ def select_group(q32_group, kseq, L, S, W, Bs, k, mode):
     summ = summarize_sequence(kseq, Bs, mode, j0, j1)
     sc = group_scores([score_blocks(q, summ, mode) for q in q32_group])
     return topk_blocks(sc, ids, k), ids, sc
+
+
+# ---------------------------------------------------------------------------
+# exact top-k inside the table candidates (reading R10)
+# ---------------------------------------------------------------------------
+
+def exact_token_topk(q32, kseq, cand_tokens, k: int):
+    """Keep the k candidate tokens with the largest exact score q . k_t
+    (canonical fp32 order of reading R4 with the key row as operand), ties to
+    the lower position; ascending.  Returns (kept positions, scores of all
+    candidates in list order)."""
+    cand = np.asarray(cand_tokens, dtype=np.int64)
+    if len(cand) == 0:
+        return cand, np.zeros(0, dtype=F32)
+    sc = canonical_dot(np.asarray(q32, dtype=F32), np.asarray(kseq, dtype=F32)[cand])
+    return topk_blocks(sc, cand, k), sc

@@ -388,3 +388,39 @@ def test_group_sum_can_overrule_a_single_head():
     grp, _, sc = orc.select_group(qs, kseq, n * Bs, 0, 16, Bs, 1, orc.SUMMARY_MEAN)
     assert own.tolist() == [5]
     assert grp.tolist() == [9]
+
+
+# ---------------------------------------------------------------------------
+# exact top-k inside the table candidates (reading R10)
+# ---------------------------------------------------------------------------
+
+def test_exact_token_topk_against_full_sort():
+    # brute force: the kept set is the k best of a full fp64 sort of the exact
+    # dot products (distinct scores), for every k
+    rng = np.random.default_rng(21)
+    D, L = 128, 300
+    kseq = orc.bf16_rne(rng.standard_normal((L, D)).astype(np.float32))
+    q = orc.bf16_rne(rng.standard_normal(D).astype(np.float32))
+    cand = np.sort(rng.choice(L, 40, replace=False))
+    exact = kseq[cand].astype(np.float64) @ q.astype(np.float64)
+    for k in range(0, 42, 3):
+        kept, sc = orc.exact_token_topk(q, kseq, cand, k)
+        assert len(sc) == len(cand)
+        want = np.sort(cand[np.argsort(-exact, kind="stable")[:min(k, len(cand))]])
+        assert np.array_equal(kept, want)
+
+
+def test_exact_token_topk_edge_cases():
+    rng = np.random.default_rng(22)
+    kseq = orc.bf16_rne(rng.standard_normal((64, 128)).astype(np.float32))
+    q = orc.bf16_rne(rng.standard_normal(128).astype(np.float32))
+    kept, sc = orc.exact_token_topk(q, kseq, np.zeros(0, np.int64), 5)
+    assert len(kept) == 0 and len(sc) == 0
+    cand = np.array([3, 9, 17])
+    kept, _ = orc.exact_token_topk(q, kseq, cand, 10)      # k beyond the list keeps it whole
+    assert kept.tolist() == [3, 9, 17]
+    # equal keys score equally: the lower position wins the tie
+    kdup = kseq.copy()
+    kdup[40] = kdup[7]
+    kept, sc = orc.exact_token_topk(q, kdup, np.array([7, 40]), 1)
+    assert sc[0] == sc[1] and kept.tolist() == [7]
