@@ -276,6 +276,24 @@ int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q,
                              float* logits_or_null, int32_t* status_or_null,
                              void* stream);
 
+/* Exact top-k inside the score-table candidates (LFPS, "The reading": an
+ * exact top-k needs a dot product against every key, the tables narrow the
+ * keys down).  For every (b, h): the candidates cand_idx[b][h][0..cand_cnt)
+ * (token positions, as sa_update_score_tables writes them) are scored by
+ * q[b][h] . k_t in the canonical fp32 order of sa_score_blocks with the bf16
+ * key row as operand; the k_per_qhead[h] best by (score descending, position
+ * ascending) are written ascending to sel_idx[b][h] (sa_sparse_decode with
+ * SA_SEL_TOKEN takes them) and their count to sel_cnt[b][h].  Entries outside
+ * [0, L) rank last.
+ * cand_idx, sel_idx: [B][Hq][kcap] int32; cand_cnt, sel_cnt: [B][Hq] int32.
+ * scores_or_null: if not NULL, [B][Hq][kcap] fp32 receives the score of every
+ * candidate at its list index.  kcap above 25600 gives SA_ERR_UNSUPPORTED. */
+int sa_select_tokens(const sa_problem* prob, const void* q, const void* k_pool,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     const int32_t* cand_idx, const int32_t* cand_cnt,
+                     int32_t* sel_idx, int32_t* sel_cnt, float* scores_or_null,
+                     void* ws, void* stream);
+
 /* Step a6 standalone -- merge two partial attentions over disjoint sets:
  * m = max(lse_a, lse_b), w_x = e^{lse_x - m},
  * o = (w_a o_a + w_b o_b) / (w_a + w_b), lse = m + log(w_a + w_b);

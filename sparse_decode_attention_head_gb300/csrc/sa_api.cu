@@ -55,6 +55,9 @@ void tables_stage_ptrs(const Params& p, void* base, int** stage, int** cnt);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
                       const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
                       int* status, int* ticket, cudaStream_t stream);
+int launch_token_topk(const Params& p, const void* q, const void* k_pool, const int* page_table, const int* seq_lens,
+                      const int* cand_idx, const int* cand_cnt, int* sel_idx, int* sel_cnt, float* scores_out,
+                      int* status, cudaStream_t stream);
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
                         const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
                         float* out, float* lse, int* status, int* ticket, cudaStream_t stream);
@@ -376,6 +379,20 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
                            at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);
+}
+
+int sa_select_tokens(const sa_problem* prob, const void* q, const void* k_pool, const int32_t* page_table,
+                     const int32_t* seq_lens, const int32_t* cand_idx, const int32_t* cand_cnt, int32_t* sel_idx,
+                     int32_t* sel_cnt, float* scores_or_null, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !page_table || !seq_lens || !cand_idx || !cand_cnt || !sel_idx || !sel_cnt || !ws)
+    return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool)) return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  return sa::launch_token_topk(p, q, k_pool, page_table, seq_lens, cand_idx, cand_cnt, sel_idx, sel_cnt,
+                               scores_or_null, at<int>(ws, l.header), as_stream(stream));
 }
 
 int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const float* slash_in, float* vert_out,

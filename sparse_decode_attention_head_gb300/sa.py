@@ -79,6 +79,7 @@ def lib():
             "sa_lse_merge": (ctypes.c_int, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_decode_step": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_select_tokens": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                       ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
         }
@@ -272,6 +273,25 @@ def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, s
         _ptr(pv.get("prev_sel_idx")), _ptr(pv.get("prev_sel_cnt")), _ptr(pv.get("prev_logits")),
         _ptr(pv.get("prev_lse")), _ptr(seq_lens), decay, beta, _ptr(cand_idx), _ptr(cand_cnt), _ptr(ws.buf),
         _stream()), "sa_update_score_tables")
+
+
+def select_tokens(prob: Problem, q, k_pool, page_table, seq_lens, cand_idx, cand_cnt, sel_idx, sel_cnt,
+                  ws: Workspace, scores=None):
+    """Exact top-k inside the score-table candidates (sa_select_tokens): the
+    k_per_head[h] best candidate tokens by the canonical fp32 q . k."""
+    _need(q, torch.bfloat16, "q", (prob.B, prob.Hq, prob.D))
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(page_table, torch.int32, "page_table", (prob.B, prob.max_pages_per_seq))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    for t, nm in ((cand_idx, "cand_idx"), (sel_idx, "sel_idx")):
+        _need(t, torch.int32, nm, (prob.B, prob.Hq, prob.kcap))
+    for t, nm in ((cand_cnt, "cand_cnt"), (sel_cnt, "sel_cnt")):
+        _need(t, torch.int32, nm, (prob.B, prob.Hq))
+    if scores is not None:
+        _need(scores, torch.float32, "scores", (prob.B, prob.Hq, prob.kcap))
+    _check(lib().sa_select_tokens(prob.ref, _ptr(q), _ptr(k_pool), _ptr(page_table), _ptr(seq_lens), _ptr(cand_idx),
+                                  _ptr(cand_cnt), _ptr(sel_idx), _ptr(sel_cnt), _ptr(scores), _ptr(ws.buf),
+                                  _stream()), "sa_select_tokens")
 
 
 def _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse):
