@@ -219,6 +219,29 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool,
                    int32_t* sel_cnt, float* out, float* lse, void* ws,
                    void* stream);
 
+/* The new token's key and value rows into the pools: for every (b, kv head)
+ * with L = seq_lens[b] > 0 (L counts the new token), k_new[b][kvh][:] and
+ * v_new[b][kvh][:] (bf16 [B][Hk][D], 16-byte aligned) are written at
+ * position L - 1, i.e. row (L - 1) % P of page page_table[b][(L - 1) / P].
+ * A page outside the pool records SA_ERR_BAD_PAGE and writes nothing.
+ * (SPIN, abstract and Fig. 6: the paged KV substrate.) */
+int sa_append_kv(const sa_problem* prob, const void* k_new, const void* v_new,
+                 void* k_pool, void* v_pool, const int32_t* page_table,
+                 const int32_t* seq_lens, void* ws, void* stream);
+
+/* sa_decode_step preceded by the append of the new token: the same results as
+ *   sa_append_kv(prob, k_new, v_new, k_pool, v_pool, page_table, seq_lens, ws, stream);
+ *   sa_decode_step(prob, q, k_pool, v_pool, page_table, seq_lens, summaries,
+ *                  sel_idx, sel_cnt, out, lse, ws, stream);
+ * with the append done inside the step (by the warp that refreshes the tail
+ * summary, after the scores, which never read the newest token's block). */
+int sa_decode_step_append(const sa_problem* prob, const void* q,
+                          const void* k_new, const void* v_new, void* k_pool,
+                          void* v_pool, const int32_t* page_table,
+                          const int32_t* seq_lens, void* summaries,
+                          int32_t* sel_idx, int32_t* sel_cnt, float* out,
+                          float* lse, void* ws, void* stream);
+
 /* Step a7 -- score-table update and table-driven candidate selection.
  * Tables: vertical (entry i = absolute position i) and slash (entry d =
  * offset d from the newest token, i.e. position L - 1 - d), fp32

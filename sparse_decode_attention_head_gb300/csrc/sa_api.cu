@@ -52,15 +52,19 @@ struct TableArgs {
 int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
 size_t tables_stage_bytes(const Params& p);
 void tables_stage_ptrs(const Params& p, void* base, int** stage, int** cnt);
-int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
-                      const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
-                      int* status, int* ticket, cudaStream_t stream);
+int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
+                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, const int* sel_cnt,
+                      void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
+                      cudaStream_t stream);
+int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table, const void* k_new, const void* v_new,
+                     void* k_pool, void* v_pool, int* status, cudaStream_t stream);
 int launch_token_topk(const Params& p, const void* q, const void* k_pool, const int* page_table, const int* seq_lens,
                       const int* cand_idx, const int* cand_cnt, int* sel_idx, int* sel_cnt, float* scores_out,
                       int* status, cudaStream_t stream);
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
-                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
-                        float* out, float* lse, int* status, int* ticket, cudaStream_t stream);
+                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, void* summ, int* sel_idx,
+                        int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
+                        cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -346,9 +350,14 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
                            at<int>(ws, l.header), tmK, tmV, nsm, s);
 }
 
-int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
-                   const int32_t* page_table, const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
-                   int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
+}  // extern "C"
+
+namespace sa_host {
+
+// sa_decode_step, and with k_new / v_new the appending variant.
+int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, const void* v_new, const void* k_pool,
+                     const void* v_pool, const int32_t* page_table, const int32_t* seq_lens, void* summaries,
+                     int32_t* sel_idx, int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
   Params p;
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
@@ -356,6 +365,8 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
       !ws)
     return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return SA_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const int nsm = num_sms_current();
@@ -367,18 +378,53 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
   cudaStream_t s = as_stream(stream);
   int* status = at<int>(ws, l.header);
   float* scores = at<float>(ws, l.scores);
+  void* kp = const_cast<void*>(k_pool);
+  void* vp = const_cast<void*>(v_pool);
+  // the scores never read the newest token's block (it is in the window), so
+  // the append and the tail summary can follow them
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
   int* ticket = at<int>(ws, l.counters) + p.B * p.Hk + 1;
-  rc = sa::launch_select_build(p, scores, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt,
+  rc = sa::launch_select_build(p, scores, seq_lens, page_table, kp, vp, k_new, v_new, summaries, sel_idx, sel_cnt,
                                at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
   if (rc == SA_ERR_UNSUPPORTED) {   // candidates beyond the fused kernel's capacity: two kernels
     if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
-    rc = sa::launch_build_step(p, seq_lens, page_table, k_pool, summaries, sel_idx, sel_cnt, at<void>(ws, l.tiles),
-                               at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+    rc = sa::launch_build_step(p, seq_lens, page_table, kp, vp, k_new, v_new, summaries, sel_idx, sel_cnt,
+                               at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
   }
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
                            at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);
+}
+
+}  // namespace sa_host
+
+extern "C" {
+
+int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
+                   const int32_t* page_table, const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
+                   int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
+  return decode_step_impl(prob, q, nullptr, nullptr, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx,
+                          sel_cnt, out, lse, ws, stream);
+}
+
+int sa_decode_step_append(const sa_problem* prob, const void* q, const void* k_new, const void* v_new, void* k_pool,
+                          void* v_pool, const int32_t* page_table, const int32_t* seq_lens, void* summaries,
+                          int32_t* sel_idx, int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
+  if (k_new == nullptr || v_new == nullptr) return SA_ERR_INVALID_ARG;
+  return decode_step_impl(prob, q, k_new, v_new, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt,
+                          out, lse, ws, stream);
+}
+
+int sa_append_kv(const sa_problem* prob, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                 const int32_t* page_table, const int32_t* seq_lens, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!k_new || !v_new || !k_pool || !v_pool || !page_table || !seq_lens || !ws) return SA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  return sa::launch_append_kv(p, seq_lens, page_table, k_new, v_new, k_pool, v_pool, at<int>(ws, l.header),
+                              as_stream(stream));
 }
 
 int sa_select_tokens(const sa_problem* prob, const void* q, const void* k_pool, const int32_t* page_table,

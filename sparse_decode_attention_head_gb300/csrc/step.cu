@@ -25,7 +25,8 @@ constexpr int kStepTileThreads = kStepBuildThreads - 32;
 
 __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
-                  const __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ summ, const int* sel_idx,
+                  __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const __nv_bfloat16* __restrict__ k_new,
+                  const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ summ, const int* sel_idx,
                   const int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
                   float* __restrict__ lse, int* status, int* ticket) {
   pdl_wait();
@@ -36,6 +37,8 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
   const int kvh = blockIdx.x, b = blockIdx.y;
   if (threadIdx.x >= kStepTileThreads) {
     const int L = min(seq_lens[b], p.mpp * kP);
+    if (k_new != nullptr)
+      append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
     if (L > 0)
       summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
     return;
@@ -47,16 +50,40 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
                                      reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
 }
 
-int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, const void* k_pool, void* summ,
-                      const int* sel_idx, const int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse,
-                      int* status, int* ticket, cudaStream_t stream) {
+int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
+                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, const int* sel_cnt,
+                      void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
+                      cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
   if (smem > 48 * 1024)
     smem_limit_at_least(reinterpret_cast<const void*>(build_step_kernel), (int)smem);
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
-                                   seq_lens, page_table, static_cast<const __nv_bfloat16*>(k_pool),
-                                   static_cast<__nv_bfloat16*>(summ), sel_idx, sel_cnt, static_cast<Tile*>(tiles),
-                                   ntiles, out, lse, status, ticket);
+                                   seq_lens, page_table, static_cast<__nv_bfloat16*>(k_pool),
+                                   static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
+                                   static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(summ),
+                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ append
+
+// One warp per (KV head, sequence): the new token's K and V rows at L - 1.
+__global__ void __launch_bounds__(32)
+append_kv_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
+                 const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                 __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, int* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int L = min(seq_lens[b], p.mpp * kP);
+  append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
+}
+
+int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table, const void* k_new, const void* v_new,
+                     void* k_pool, void* v_pool, int* status, cudaStream_t stream) {
+  const cudaError_t e = launch_pdl(append_kv_kernel, dim3(p.Hk, p.B), dim3(32), 0, stream, p, seq_lens, page_table,
+                                   static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+                                   static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool), status);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -71,7 +98,8 @@ int launch_build_step(const Params& p, const int* seq_lens, const int* page_tabl
 template <int GROUP, int KPT>
 __global__ void __launch_bounds__(kStepBuildThreads)
 select_build_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
-                    const int* __restrict__ page_table, const __nv_bfloat16* __restrict__ k_pool,
+                    const int* __restrict__ page_table, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
+                    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
                     __nv_bfloat16* __restrict__ summ, int* __restrict__ sel_idx, int* __restrict__ sel_cnt,
                     Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
                     float* __restrict__ lse, int* status, int* ticket) {
@@ -108,6 +136,8 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
     if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
   if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
   if (tid >= kStepTileThreads) {
+    if (k_new != nullptr)
+      append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
     if (L > 0)
       summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
     return;
@@ -120,14 +150,15 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
 // key capacity or its shared memory would not fit; the caller then runs
 // topk_kernel + build_step_kernel.
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
-                        const void* k_pool, void* summ, int* sel_idx, int* sel_cnt, void* tiles, int* ntiles,
-                        float* out, float* lse, int* status, int* ticket, cudaStream_t stream) {
+                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, void* summ, int* sel_idx,
+                        int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
+                        cudaStream_t stream) {
   int max_n = 0;
   for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
   const size_t smem = build_smem_bytes(p.mpp) + ((size_t)p.G * p.kcap + p.G) * sizeof(int);
   if (smem > 160 * 1024) return SA_ERR_UNSUPPORTED;
-  void (*kern)(Params, const float*, const int*, const int*, const __nv_bfloat16*, __nv_bfloat16*, int*, int*,
-               Tile*, int*, float*, float*, int*, int*) = nullptr;
+  void (*kern)(Params, const float*, const int*, const int*, __nv_bfloat16*, __nv_bfloat16*, const __nv_bfloat16*,
+               const __nv_bfloat16*, __nv_bfloat16*, int*, int*, Tile*, int*, float*, float*, int*, int*) = nullptr;
   if (p.G <= 4) {
     if (max_n <= 256 * 8) kern = select_build_kernel<256, 8>;
     else if (max_n <= 256 * 16) kern = select_build_kernel<256, 16>;
@@ -137,9 +168,10 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
   if (kern == nullptr) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024) smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
   const cudaError_t e = launch_pdl(kern, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p, scores, seq_lens,
-                                   page_table, static_cast<const __nv_bfloat16*>(k_pool),
-                                   static_cast<__nv_bfloat16*>(summ), sel_idx, sel_cnt, static_cast<Tile*>(tiles),
-                                   ntiles, out, lse, status, ticket);
+                                   page_table, static_cast<__nv_bfloat16*>(k_pool),
+                                   static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
+                                   static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(summ),
+                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

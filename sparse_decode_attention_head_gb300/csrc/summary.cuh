@@ -7,8 +7,10 @@
 namespace sa {
 
 // Warp-collective: summary of block j of (b, kvh) over tokens [j Bs, min((j+1) Bs, L)).
+// Plain (coherent) loads, no __restrict__: in a decode step the same kernel
+// may have just written the block's newest row (append_token_warp).
 __device__ __forceinline__ void summarize_block_warp(const Params& p, int b, int kvh, int j, int L,
-                                                     const __nv_bfloat16* __restrict__ k_pool,
+                                                     const __nv_bfloat16* k_pool,
                                                      const int* __restrict__ pt, __nv_bfloat16* __restrict__ summ,
                                                      int* status) {
   const int lane = threadIdx.x & 31;
@@ -36,7 +38,7 @@ __device__ __forceinline__ void summarize_block_warp(const Params& p, int b, int
     uint2 v[kP];
 #pragma unroll
     for (int r = 0; r < kP; ++r)
-      if (r < rows) v[r] = __ldg(src + r * (kD / 4));
+      if (r < rows) v[r] = src[r * (kD / 4)];
 #pragma unroll
     for (int r = 0; r < kP; ++r) {
       if (r < rows) {
@@ -81,6 +83,28 @@ __device__ __forceinline__ void summarize_block_warp(const Params& p, int b, int
     }
     reinterpret_cast<uint2*>(summ + (unit_slot + j) * kD)[lane] = o;
   }
+}
+
+// Warp-collective: write the new token's key and value rows (k_new / v_new
+// [B][Hk][D] bf16) at position L - 1 of (b, kvh), through the page table.
+// The warp's later reads of the row (the tail summary) see the writes.
+__device__ __forceinline__ void append_token_warp(const Params& p, int b, int kvh, int L,
+                                                  const __nv_bfloat16* __restrict__ k_new,
+                                                  const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* k_pool,
+                                                  __nv_bfloat16* v_pool, const int* __restrict__ pt, int* status) {
+  const int lane = threadIdx.x & 31;
+  if (L <= 0) return;
+  const int t = L - 1;
+  const int phys = pt[t / kP];
+  if (phys < 0 || phys >= p.num_pages) {
+    if (lane == 0) set_status(status, SA_ERR_BAD_PAGE);
+    return;
+  }
+  const size_t src = ((size_t)b * p.Hk + kvh) * kD;
+  const size_t dst = (((size_t)phys * p.Hk + kvh) * kP + t % kP) * kD;
+  reinterpret_cast<uint2*>(k_pool + dst)[lane] = reinterpret_cast<const uint2*>(k_new + src)[lane];
+  reinterpret_cast<uint2*>(v_pool + dst)[lane] = reinterpret_cast<const uint2*>(v_new + src)[lane];
+  __syncwarp();
 }
 
 }  // namespace sa

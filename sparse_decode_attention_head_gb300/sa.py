@@ -80,6 +80,8 @@ def lib():
             "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_decode_step": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_select_tokens": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_append_kv": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_decode_step_append": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                       ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
         }
@@ -315,6 +317,30 @@ def decode_step(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summarie
     _check(lib().sa_decode_step(prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens),
                                 _ptr(summaries), _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf),
                                 _stream()), "sa_decode_step")
+
+
+def append_kv(prob: Problem, k_new, v_new, k_pool, v_pool, page_table, seq_lens, ws: Workspace):
+    """The new token's K and V rows into the pools at position seq_lens[b] - 1 (sa_append_kv)."""
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, nm, (prob.B, prob.Hk, prob.D))
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool", tuple(k_pool.shape))
+    _need(page_table, torch.int32, "page_table", (prob.B, prob.max_pages_per_seq))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    _check(lib().sa_append_kv(prob.ref, _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                              _ptr(seq_lens), _ptr(ws.buf), _stream()), "sa_append_kv")
+
+
+def decode_step_append(prob: Problem, q, k_new, v_new, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx,
+                       sel_cnt, out, lse, ws: Workspace):
+    """The new token's K/V appended, then the whole decode step (sa_decode_step_append)."""
+    _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse)
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, nm, (prob.B, prob.Hk, prob.D))
+    _check(lib().sa_decode_step_append(prob.ref, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                       _ptr(page_table), _ptr(seq_lens), _ptr(summaries), _ptr(sel_idx),
+                                       _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf), _stream()),
+           "sa_decode_step_append")
 
 
 class DecodeStepCall:
