@@ -28,7 +28,9 @@ Sources (page title, section / equation / figure):
   * "Learn from the Past: Fast Sparse Indexing for Large Language Model
     Decoding" (LFPS), "What carries the argument", Eq. (9), Eq. (10): vertical
     and slash score tables with decay r = 0.95 and positional expansion by
-    offsets {-1, 0, 1, 2}.
+    offsets {-1, 0, 1, 2}; Algorithm 1 step 1, Eq. (5), Eq. (6), App. B.1
+    ("Assumptions & free parameters"): the head-sparsity estimate and the
+    mean-value bypass with epsilon = 0.85.
 
 Readings where the pages are silent (each also listed in the design notes):
   R1  I = sinks [0, min(S, L)) U window [max(L - W, min(S, L)), L);
@@ -58,6 +60,14 @@ Readings where the pages are silent (each also listed in the design notes):
       blocks of a KV head are ranked by the fp32 sum, in head order, of its G
       query heads' canonical scores; every head of the group keeps the same k
       blocks (ties by lower block index).
+  R11 Head-sparsity bypass (LFPS Algorithm 1 step 1, Eq. (5), Eq. (6),
+      App. B.1; epsilon = 0.85): tokens split into the sink (token 0), the
+      local window (the six newest of the L keys) and the n global tokens
+      between; the global mass is n times the log-normal mean of e^z with the
+      page's sigma^2 read as the keys' mean per-dimension variance times the
+      softmax scale squared.  rho = sink mass / total; rho > epsilon bypasses
+      the head: output the mean value row over all L tokens, lse = log of the
+      total mass, and the head's score tables skip the next update.
 """
 from __future__ import annotations
 
@@ -420,3 +430,65 @@ def exact_token_topk(q32, kseq, cand_tokens, k: int):
         return cand, np.zeros(0, dtype=F32)
     sc = canonical_dot(np.asarray(q32, dtype=F32), np.asarray(kseq, dtype=F32)[cand])
     return topk_blocks(sc, cand, k), sc
+
+
+# ---------------------------------------------------------------------------
+# variant: head-sparsity estimate and mean-value bypass (reading R11)
+# ---------------------------------------------------------------------------
+
+# LFPS, "Assumptions & free parameters": sparsity threshold epsilon = 0.85 and
+# a local window of six recent tokens in Eq. (5).
+BYPASS_EPS = 0.85
+LOCAL_WINDOW = 6
+
+
+def sparsity_partition(L: int):
+    """Token classes of the estimate (reading R11): the sink token 0, the
+    local tokens [max(1, L - 6), L) and the n global tokens [1, max(1, L - 6)).
+    Returns (local positions, global positions)."""
+    if L <= 0:
+        return np.zeros(0, dtype=np.int64), np.zeros(0, dtype=np.int64)
+    lo = max(1, L - LOCAL_WINDOW)
+    return np.arange(lo, L, dtype=np.int64), np.arange(1, lo, dtype=np.int64)
+
+
+def head_sparsity(q, kseq, L: int, scale: float):
+    """LFPS's sink-proportion estimate for one query head (Eq. (5), Eq. (6),
+    App. B.1 as read in R11), fp64.
+
+    z_t = scale * q . k_t.  Sink mass e^{z_0}; local mass the sum of e^{z_t}
+    over the local tokens; global mass n * exp(scale q . Kbar + scale^2 |q|^2
+    sigma^2 / 2), the mean of e^z under independent normal key components
+    with the global tokens' mean Kbar and mean per-dimension population
+    variance sigma^2.  Returns (rho, lse_est): the sink's share of the three
+    masses and the log of their sum.  L = 0 gives (0, -inf)."""
+    if L <= 0:
+        return 0.0, -math.inf
+    q = np.asarray(q, dtype=F64)
+    K = np.asarray(kseq[:L], dtype=F64)
+    loc, glo = sparsity_partition(L)
+    logs = [scale * float(K[0] @ q)]                      # the sink
+    logs += [scale * float(K[t] @ q) for t in loc]
+    n = len(glo)
+    if n > 0:
+        Kg = K[glo]
+        kbar = Kg.mean(axis=0)
+        var = ((Kg - kbar[None, :]) ** 2).mean(axis=0).mean()
+        logs.append(math.log(n) + scale * float(kbar @ q) + 0.5 * scale * scale * float(q @ q) * var)
+    m = max(logs)
+    tot = sum(math.exp(x - m) for x in logs)
+    return math.exp(logs[0] - m) / tot, m + math.log(tot)
+
+
+def bypass_output(vseq, L: int) -> np.ndarray:
+    """Output of a bypassed head (LFPS Algorithm 1, step 1): the mean value
+    row over the L tokens, fp64.  L = 0 gives zeros."""
+    D = vseq.shape[1]
+    if L <= 0:
+        return np.zeros(D, dtype=F64)
+    return np.asarray(vseq[:L], dtype=F64).mean(axis=0)
+
+
+def is_bypassed(rho: float, eps: float = BYPASS_EPS) -> bool:
+    """A head is bypassed when its sink share exceeds epsilon (strict)."""
+    return rho > eps
