@@ -195,13 +195,17 @@ int sa_select_topk(const sa_problem* prob, const void* q,
  * logits_or_null: if not NULL, [B][Hq][max_pages_per_seq*P] fp32 receives the
  *   natural-log-domain logit z_t at every attended position t (other positions
  *   untouched).  Used to feed the score-table update.
+ * bypass_or_null: if not NULL, [B][Hq] int32 as sa_head_sparsity writes it:
+ *   a head with a non-zero entry is left out (its selection ignored, no KV
+ *   read for it alone) and its out / lse rows are not written.
  * out: [B][Hq][D] fp32; lse: [B][Hq] fp32 (natural log). */
 int sa_sparse_decode(const sa_problem* prob, const void* q,
                      const void* k_pool, const void* v_pool,
                      const int32_t* page_table, const int32_t* seq_lens,
                      const int32_t* sel_idx, const int32_t* sel_cnt,
                      int32_t sel_granularity, float* out, float* lse,
-                     float* logits_or_null, void* ws, void* stream);
+                     float* logits_or_null, const int32_t* bypass_or_null,
+                     void* ws, void* stream);
 
 /* One whole decode step for block selection -- a1 (incremental) + a2 + a3 +
  * a4 + a5 + a6: the same results as
@@ -254,7 +258,10 @@ int sa_decode_step_append(const sa_problem* prob, const void* q,
  *   T_out = fma(decay, T_in, (1 - decay) * exp(z - lse))   (attended)
  *   T_out = decay * T_in                                 (not attended)
  * in fp32; the slash entry d takes the weight of position Lp - 1 - d.
- * Without prev_logits the tables are copied unchanged.
+ * Without prev_logits the tables are copied unchanged; so are the rows of
+ * heads with a non-zero prev_bypass_or_null[b][h] ([B][Hq] int32, the
+ * previous step's sa_head_sparsity flags: LFPS leaves a bypassed head's
+ * tables as they were).
  * Selection for the next step of length L = seq_lens[b]: position i in the
  * middle region M of L is a seed if vert_out[i] > tau or slash_out[L-1-i] >
  * tau, tau = beta / |I(L)| (fp32, strict); candidates are the seeds expanded
@@ -269,6 +276,7 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in,
                            const int32_t* prev_sel_idx,
                            const int32_t* prev_sel_cnt,
                            const float* prev_logits, const float* prev_lse,
+                           const int32_t* prev_bypass_or_null,
                            const int32_t* seq_lens, float decay, float beta,
                            int32_t* cand_idx, int32_t* cand_cnt, void* ws,
                            void* stream);
@@ -316,6 +324,59 @@ int sa_select_tokens(const sa_problem* prob, const void* q, const void* k_pool,
                      const int32_t* cand_idx, const int32_t* cand_cnt,
                      int32_t* sel_idx, int32_t* sel_cnt, float* scores_or_null,
                      void* ws, void* stream);
+
+/* Head-sparsity bypass (LFPS, "Learn from the Past": Algorithm 1 step 1,
+ * Eq. (5), Eq. (6), App. B.1, epsilon = 0.85).  A variant, off unless these
+ * calls are made.
+ *
+ * kv_stats: [B][Hk][3][D] fp32, per (b, kv head) the sums over the L =
+ * seq_lens[b] cached tokens of k, of k*k (per dimension) and of v; 16-byte
+ * aligned.  sa_kv_stats computes them from the cache in one pass (sums in
+ * fp32, in a fixed order); sa_decode_step_bypass with k_new keeps them
+ * current as tokens are appended.
+ *
+ * sa_head_sparsity: for every (b, h) with logits z_t = scale q . k_t, the
+ * sink token 0, the local window [max(1, L - 6), L) and the n = max(0, L - 7)
+ * global tokens between:
+ *   m_sink = e^{z_0}, m_local = sum over the window of e^{z_t},
+ *   m_global = n exp(scale q . Kbar + scale^2 |q|^2 sigma^2 / 2)
+ * with Kbar the global keys' mean and sigma^2 the mean over dims of their
+ * per-dim variance (from kv_stats minus the sink and window rows) -- the
+ * log-normal mean of e^z.  rho = m_sink / (m_sink + m_local + m_global)
+ * (fp32) goes to rho_or_null[b][h]; bypass[b][h] = rho > eps (0 <= eps <= 1,
+ * else SA_ERR_INVALID_ARG).  For a bypassed head out[b][h][:] = sum v / L and
+ * lse[b][h] = log(m_sink + m_local + m_global); other rows of out / lse are
+ * not touched.  L = 0 is never bypassed.  A page outside the pool records
+ * SA_ERR_BAD_PAGE and leaves the head unbypassed.
+ * rho_or_null: [B][Hq] fp32; bypass: [B][Hq] int32; out: [B][Hq][D] fp32,
+ * lse: [B][Hq] fp32 (16-byte aligned out). */
+int sa_kv_stats(const sa_problem* prob, const void* k_pool, const void* v_pool,
+                const int32_t* page_table, const int32_t* seq_lens,
+                float* kv_stats, void* ws, void* stream);
+
+int sa_head_sparsity(const sa_problem* prob, const void* q, const void* k_pool,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     const float* kv_stats, float eps, float* rho_or_null,
+                     int32_t* bypass, float* out, float* lse, void* ws,
+                     void* stream);
+
+/* The decode step with the bypass: the same results as
+ *   [sa_append_kv(...) and the new rows added to kv_stats, when k_new_or_null]
+ *   sa_head_sparsity(prob, q, k_pool, page_table, seq_lens, kv_stats, eps,
+ *                    rho_or_null, bypass, out, lse, ws, stream);
+ *   sa_decode_step(...)   with the bypassed heads left out:
+ * a bypassed head gets sel_cnt = 0, no KV is read for it alone, and its out /
+ * lse rows keep the bypass output.  k_new_or_null and v_new_or_null are both
+ * NULL or both set (bf16 [B][Hk][D]; then L = seq_lens[b] counts the new
+ * token and kv_stats must cover the L - 1 tokens before it on entry). */
+int sa_decode_step_bypass(const sa_problem* prob, const void* q,
+                          const void* k_new_or_null, const void* v_new_or_null,
+                          void* k_pool, void* v_pool,
+                          const int32_t* page_table, const int32_t* seq_lens,
+                          void* summaries, float* kv_stats, float eps,
+                          int32_t* sel_idx, int32_t* sel_cnt, float* out,
+                          float* lse, float* rho_or_null, int32_t* bypass,
+                          void* ws, void* stream);
 
 /* Step a6 standalone -- merge two partial attentions over disjoint sets:
  * m = max(lse_a, lse_b), w_x = e^{lse_x - m},

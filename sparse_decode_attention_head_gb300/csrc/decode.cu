@@ -617,6 +617,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       }
       if (whole) {
         const size_t row = (size_t)b * p.Hq + kvh * G + g;
+        if (p.bypass != nullptr && p.bypass[row]) continue;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         *reinterpret_cast<float4*>(A.out + row * kD + 4 * lane) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -689,6 +690,7 @@ merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __r
   }
   const int b = u / p.Hk, kvh = u % p.Hk;
   const size_t row = (size_t)b * p.Hq + kvh * G + g;
+  if (p.bypass != nullptr && p.bypass[row]) return;
   out[row * kD + tid] = l > 0.f ? acc / l : 0.f;
   if (tid == 0) lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
 }

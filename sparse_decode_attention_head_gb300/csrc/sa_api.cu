@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "sa_common.cuh"
+#include "tables.cuh"
 
 namespace sa {
 int launch_summarize(const Params& p, const void* k_pool, const int* page_table, const int* seq_lens,
@@ -30,30 +31,8 @@ size_t decode_partials_bytes(const Params& p);
 size_t tiles_bytes(const Params& p);
 int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                      const float* lse_b, float* o, float* lse, cudaStream_t stream);
-struct TableArgs {
-  const float* vin;
-  const float* sin;
-  float* vout;
-  float* sout;
-  const int* prev_lens;
-  const int* prev_sel;
-  const int* prev_cnt;
-  const float* prev_logits;
-  const float* prev_lse;
-  const int* lens;
-  int* cand;
-  int* cand_cnt;
-  int* stage;
-  int* stage_cnt;
-  int* status;
-  float decay;
-  float beta;
-};
-int launch_tables(const Params& p, const TableArgs& A, cudaStream_t stream);
-size_t tables_stage_bytes(const Params& p);
-void tables_stage_ptrs(const Params& p, void* base, int** stage, int** cnt);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
-                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, const int* sel_cnt,
+                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, int* sel_cnt,
                       void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                       cudaStream_t stream);
 int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table, const void* k_new, const void* v_new,
@@ -65,6 +44,11 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
                         void* k_pool, void* v_pool, const void* k_new, const void* v_new, void* summ, int* sel_idx,
                         int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                         cudaStream_t stream);
+int launch_kv_stats(const Params& p, const void* k_pool, const void* v_pool, const int* page_table,
+                    const int* seq_lens, float* stats, int* status, cudaStream_t stream);
+int launch_sparsity(const Params& p, const void* q, void* k_pool, void* v_pool, const int* page_table,
+                    const int* seq_lens, const void* k_new, const void* v_new, float* stats, float eps, float* rho,
+                    int* bypass, float* out, float* lse, int* status, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -324,10 +308,11 @@ int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries,
 int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel_idx,
                      const int32_t* sel_cnt, int32_t sel_granularity, float* out, float* lse,
-                     float* logits_or_null, void* ws, void* stream) {
+                     float* logits_or_null, const int32_t* bypass_or_null, void* ws, void* stream) {
   Params p;
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
+  p.bypass = bypass_or_null;
   if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !sel_idx || !sel_cnt || !out || !lse || !ws)
     return SA_ERR_INVALID_ARG;
   if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
@@ -355,12 +340,16 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
 namespace sa_host {
 
 // sa_decode_step, and with k_new / v_new the appending variant.
+// With kv_stats the step starts with the sparsity estimate (which then also
+// does the append) and leaves the bypassed heads out of everything after it.
 int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, const void* v_new, const void* k_pool,
                      const void* v_pool, const int32_t* page_table, const int32_t* seq_lens, void* summaries,
-                     int32_t* sel_idx, int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
+                     int32_t* sel_idx, int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream,
+                     float* kv_stats = nullptr, float eps = 1.f, float* rho = nullptr, int32_t* bypass = nullptr) {
   Params p;
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
+  if (kv_stats != nullptr && (bypass == nullptr || !(eps >= 0.f && eps <= 1.f))) return SA_ERR_INVALID_ARG;
   if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !summaries || !sel_idx || !sel_cnt || !out || !lse ||
       !ws)
     return SA_ERR_INVALID_ARG;
@@ -380,6 +369,13 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   float* scores = at<float>(ws, l.scores);
   void* kp = const_cast<void*>(k_pool);
   void* vp = const_cast<void*>(v_pool);
+  if (kv_stats != nullptr) {
+    rc = sa::launch_sparsity(p, q, kp, vp, page_table, seq_lens, k_new, v_new, kv_stats, eps, rho, bypass, out, lse,
+                             status, s);
+    if (rc != SA_OK) return rc;
+    p.bypass = bypass;
+    k_new = v_new = nullptr;   // appended above
+  }
   // the scores never read the newest token's block (it is in the window), so
   // the append and the tail summary can follow them
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
@@ -415,6 +411,45 @@ int sa_decode_step_append(const sa_problem* prob, const void* q, const void* k_n
                           out, lse, ws, stream);
 }
 
+int sa_decode_step_bypass(const sa_problem* prob, const void* q, const void* k_new_or_null,
+                          const void* v_new_or_null, void* k_pool, void* v_pool, const int32_t* page_table,
+                          const int32_t* seq_lens, void* summaries, float* kv_stats, float eps, int32_t* sel_idx,
+                          int32_t* sel_cnt, float* out, float* lse, float* rho_or_null, int32_t* bypass, void* ws,
+                          void* stream) {
+  if (kv_stats == nullptr || bypass == nullptr || !aligned16(kv_stats)) return SA_ERR_INVALID_ARG;
+  return decode_step_impl(prob, q, k_new_or_null, v_new_or_null, k_pool, v_pool, page_table, seq_lens, summaries,
+                          sel_idx, sel_cnt, out, lse, ws, stream, kv_stats, eps, rho_or_null, bypass);
+}
+
+int sa_kv_stats(const sa_problem* prob, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                const int32_t* seq_lens, float* kv_stats, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!k_pool || !v_pool || !page_table || !seq_lens || !kv_stats || !ws) return SA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(kv_stats)) return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  return sa::launch_kv_stats(p, k_pool, v_pool, page_table, seq_lens, kv_stats, at<int>(ws, l.header),
+                             as_stream(stream));
+}
+
+int sa_head_sparsity(const sa_problem* prob, const void* q, const void* k_pool, const int32_t* page_table,
+                     const int32_t* seq_lens, const float* kv_stats, float eps, float* rho_or_null, int32_t* bypass,
+                     float* out, float* lse, void* ws, void* stream) {
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !page_table || !seq_lens || !kv_stats || !bypass || !out || !lse || !ws)
+    return SA_ERR_INVALID_ARG;
+  if (!(eps >= 0.f && eps <= 1.f)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(kv_stats) || !aligned16(out)) return SA_ERR_INVALID_ARG;
+  const Layout l = layout_of(p);
+  // without k_new the kernel neither writes the pools nor the sums
+  return sa::launch_sparsity(p, q, const_cast<void*>(k_pool), nullptr, page_table, seq_lens, nullptr, nullptr,
+                             const_cast<float*>(kv_stats), eps, rho_or_null, bypass, out, lse,
+                             at<int>(ws, l.header), as_stream(stream));
+}
+
 int sa_append_kv(const sa_problem* prob, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                  const int32_t* page_table, const int32_t* seq_lens, void* ws, void* stream) {
   Params p;
@@ -444,8 +479,8 @@ int sa_select_tokens(const sa_problem* prob, const void* q, const void* k_pool, 
 int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const float* slash_in, float* vert_out,
                            float* slash_out, const int32_t* prev_seq_lens, const int32_t* prev_sel_idx,
                            const int32_t* prev_sel_cnt, const float* prev_logits, const float* prev_lse,
-                           const int32_t* seq_lens, float decay, float beta, int32_t* cand_idx, int32_t* cand_cnt,
-                           void* ws, void* stream) {
+                           const int32_t* prev_bypass_or_null, const int32_t* seq_lens, float decay, float beta,
+                           int32_t* cand_idx, int32_t* cand_cnt, void* ws, void* stream) {
   Params p;
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
@@ -474,6 +509,7 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in, const f
   A.prev_cnt = prev_sel_cnt;
   A.prev_logits = prev_logits;
   A.prev_lse = prev_lse;
+  A.frozen = prev_bypass_or_null;
   A.lens = seq_lens;
   A.cand = cand_idx;
   A.cand_cnt = cand_cnt;

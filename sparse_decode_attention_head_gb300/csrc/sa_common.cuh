@@ -28,6 +28,7 @@ struct Params {
   int slots;        // block slots per (b, kvh)
   float scale;
   int sel_mode;     // SA_SELECT_*
+  const int* bypass;  // [B][Hq] non-zero: the head was answered by the sparsity bypass (NULL: none)
   int bs[SA_MAX_HK];
   int k[SA_MAX_HQ];
 };

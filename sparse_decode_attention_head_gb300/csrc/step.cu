@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                   __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const __nv_bfloat16* __restrict__ k_new,
                   const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ summ, const int* sel_idx,
-                  const int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
+                  int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
                   float* __restrict__ lse, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
@@ -48,10 +48,13 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
   build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0,
                                      SA_SEL_BLOCK, tiles, ntiles, out, lse, status, smem_b,
                                      reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
+  // the builder's reads of the counts ended at its last barrier: heads
+  // answered by the sparsity bypass report no selection
+  if (p.bypass != nullptr && threadIdx.x < p.G && p.bypass[h0 + threadIdx.x]) sel_cnt[h0 + threadIdx.x] = 0;
 }
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
-                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, const int* sel_cnt,
+                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, int* sel_cnt,
                       void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                       cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
@@ -132,9 +135,11 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   }
   __syncthreads();
   const size_t h0 = (size_t)b * p.Hq + kvh * G;
+  // heads answered by the sparsity bypass select nothing (the builder skips them)
+  auto bypassed = [&](int gg) { return p.bypass != nullptr && p.bypass[h0 + gg] != 0; };
   for (int i = tid; i < G * p.kcap; i += kStepBuildThreads)
-    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
-  if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
+    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap] && !bypassed(i / p.kcap)) sel_idx[h0 * p.kcap + i] = s_sel[i];
+  if (tid < G) sel_cnt[h0 + tid] = bypassed(tid) ? 0 : s_cnt[tid];
   if (tid >= kStepTileThreads) {
     if (k_new != nullptr)
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);

@@ -25,7 +25,7 @@
 // has already rewritten.
 #include <algorithm>
 
-#include "sa_common.cuh"
+#include "tables.cuh"
 
 namespace sa {
 
@@ -34,25 +34,6 @@ constexpr int kPer = 8;                        // positions per thread per chunk
 constexpr int kChunk = kTabThreads * kPer;     // 4096
 constexpr int kHalo = 3;                       // seeds at i-2 .. i+1 expand onto i
 
-struct TableArgs {
-  const float* vin;
-  const float* sin;
-  float* vout;
-  float* sout;
-  const int* prev_lens;
-  const int* prev_sel;
-  const int* prev_cnt;
-  const float* prev_logits;
-  const float* prev_lse;
-  const int* lens;
-  int* cand;
-  int* cand_cnt;
-  int* stage;      // [B * Hq][nchunks][min(kChunk, kcap)] candidates of each chunk
-  int* stage_cnt;  // [B * Hq][nchunks]
-  int* status;
-  float decay;
-  float beta;
-};
 
 // Weight fed to the tables by an entry the previous step attended:
 // (1 - r) e^(z - lse), z its logit.
@@ -87,7 +68,7 @@ tables_kernel(Params p, TableArgs A) {
   const int n_dense = s_end + (L - w_beg);
   const float tau = n_dense > 0 ? __fdiv_rn(A.beta, (float)n_dense) : INFINITY;
   const float r = A.decay, one_minus_r = __fsub_rn(1.0f, A.decay);
-  const bool has_prev = A.prev_logits != nullptr;
+  const bool has_prev = A.prev_logits != nullptr && !(A.frozen != nullptr && A.frozen[(size_t)b * p.Hq + h]);
   int Lp = 0, ps_end = 0, pw_beg = 0, scnt = 0;
   float lse = 0.f;
   const int* sel = nullptr;

@@ -43,7 +43,8 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
 // then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
 // a block scan of the page flags, and one 32-byte store per tile.
 // sel_row: the unit's selections [G][kcap] (global or shared memory),
-// cnt_row: their counts [G].  s_flag: window ints, s_mask: 4 window words,
+// cnt_row: their counts [G].  Heads flagged in p.bypass are left out: no
+// tokens attend for them and their output rows are not written.  s_flag: window ints, s_mask: 4 window words,
 // scan_tmp: 32 ints.
 template <int NT>
 __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh, const int* __restrict__ seq_lens,
@@ -63,6 +64,10 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   const int per = (win + NT - 1) / NT;
   // ---- up-front loads
   const int Lraw = seq_lens[b];
+  uint32_t active = (1u << p.G) - 1u;   // heads whose rows this unit writes
+  if (p.bypass != nullptr)
+    for (int g = 0; g < p.G; ++g)
+      if (p.bypass[(size_t)b * p.Hq + kvh * p.G + g]) active &= ~(1u << g);
   int ptr[kPer];
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
@@ -87,7 +92,7 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   int s_end, w_beg;
   partition(Lc, p.S, p.W, s_end, w_beg);
   const int Bs = p.bs[kvh];
-  const uint32_t all = (1u << G) - 1u;
+  const uint32_t all = active;
   Tile* T = tiles + (size_t)u * p.mpp;
   int total = 0;
 
@@ -126,7 +131,7 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
         cnt = cnt_row[g];
         x = sel_row[it];
       }
-      if (i >= min(cnt, p.kcap)) continue;
+      if (i >= min(cnt, p.kcap) || !((active >> g) & 1u)) continue;
       int lo, hi;
       item_range(gran, x, Bs, Lc, s_end, w_beg, lo, hi);
       lo = max(lo, tlo);
@@ -180,8 +185,9 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   }
   if (tid == 0) ntiles[u] = total;
   if (total == 0) {   // nothing attended (L = 0): O = 0, lse = -inf; the decode kernel skips the unit
-    for (int i = tid; i < G * kD; i += NT) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
-    if (tid < G) lse[(size_t)b * p.Hq + kvh * G + tid] = -INFINITY;
+    for (int i = tid; i < G * kD; i += NT)
+      if ((active >> (i / kD)) & 1u) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
+    if (tid < G && ((active >> tid) & 1u)) lse[(size_t)b * p.Hq + kvh * G + tid] = -INFINITY;
   }
 }
 

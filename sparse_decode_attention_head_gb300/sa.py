@@ -75,15 +75,19 @@ def lib():
             "sa_block_summarize": (ctypes.c_int, [P, vp, vp, vp, i32, i32, vp, vp, vp]),
             "sa_score_blocks": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp]),
             "sa_select_topk": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp]),
-            "sa_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
+            "sa_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
             "sa_lse_merge": (ctypes.c_int, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "sa_sparse_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
             "sa_decode_step": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_select_tokens": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_append_kv": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp]),
             "sa_decode_step_append": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
-            "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+            "sa_update_score_tables": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                       ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
+            "sa_kv_stats": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_head_sparsity": (ctypes.c_int, [P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp]),
+            "sa_decode_step_bypass": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                                     vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -224,7 +228,9 @@ def select_topk(prob: Problem, q, summaries, seq_lens, sel_idx, sel_cnt, ws: Wor
 
 
 def sparse_decode(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, sel_idx, sel_cnt, out, lse,
-                  ws: Workspace, granularity: int = SEL_BLOCK, logits=None):
+                  ws: Workspace, granularity: int = SEL_BLOCK, logits=None, bypass=None):
+    """bypass: optional [B][Hq] int32 flags of sa_head_sparsity; flagged heads
+    are left out and their out / lse rows are not written."""
     _need(q, torch.bfloat16, "q", (prob.B, prob.Hq, prob.D))
     _need(k_pool, torch.bfloat16, "k_pool")
     _need(v_pool, torch.bfloat16, "v_pool", tuple(k_pool.shape))
@@ -238,9 +244,12 @@ def sparse_decode(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, sel_id
     _need(lse, torch.float32, "lse", (prob.B, prob.Hq))
     if logits is not None:
         _need(logits, torch.float32, "logits", (prob.B, prob.Hq, prob.max_pages_per_seq * prob.page_size))
+    if bypass is not None:
+        _need(bypass, torch.int32, "bypass", (prob.B, prob.Hq))
     _check(lib().sa_sparse_decode(prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
                                   _ptr(seq_lens), _ptr(sel_idx), _ptr(sel_cnt), granularity, _ptr(out),
-                                  _ptr(lse), _ptr(logits), _ptr(ws.buf), _stream()), "sa_sparse_decode")
+                                  _ptr(lse), _ptr(logits), _ptr(bypass), _ptr(ws.buf), _stream()),
+           "sa_sparse_decode")
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b, o, lse):
@@ -254,9 +263,11 @@ def lse_merge(o_a, lse_a, o_b, lse_b, o, lse):
 
 
 def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, seq_lens, cand_idx, cand_cnt,
-                        ws: Workspace, decay: float = 0.95, beta: float = 1.0, prev=None):
+                        ws: Workspace, decay: float = 0.95, beta: float = 1.0, prev=None, prev_bypass=None):
     """prev: None (first step: tables copied) or a dict with prev_seq_lens,
-    prev_sel_idx, prev_sel_cnt, prev_logits, prev_lse of the previous step."""
+    prev_sel_idx, prev_sel_cnt, prev_logits, prev_lse of the previous step.
+    prev_bypass: optional [B][Hq] int32 flags of the previous step's
+    sa_head_sparsity; the tables of flagged heads are copied unchanged."""
     N = prob.max_pages_per_seq * prob.page_size
     for t, nm in ((vert_in, "vert_in"), (slash_in, "slash_in"), (vert_out, "vert_out"), (slash_out, "slash_out")):
         _need(t, torch.float32, nm, (prob.B, prob.Hq, N))
@@ -270,10 +281,12 @@ def update_score_tables(prob: Problem, vert_in, slash_in, vert_out, slash_out, s
         _need(pv["prev_sel_cnt"], torch.int32, "prev_sel_cnt", (prob.B, prob.Hq))
         _need(pv["prev_logits"], torch.float32, "prev_logits", (prob.B, prob.Hq, N))
         _need(pv["prev_lse"], torch.float32, "prev_lse", (prob.B, prob.Hq))
+    if prev_bypass is not None:
+        _need(prev_bypass, torch.int32, "prev_bypass", (prob.B, prob.Hq))
     _check(lib().sa_update_score_tables(
         prob.ref, _ptr(vert_in), _ptr(slash_in), _ptr(vert_out), _ptr(slash_out), _ptr(pv.get("prev_seq_lens")),
         _ptr(pv.get("prev_sel_idx")), _ptr(pv.get("prev_sel_cnt")), _ptr(pv.get("prev_logits")),
-        _ptr(pv.get("prev_lse")), _ptr(seq_lens), decay, beta, _ptr(cand_idx), _ptr(cand_cnt), _ptr(ws.buf),
+        _ptr(pv.get("prev_lse")), _ptr(prev_bypass), _ptr(seq_lens), decay, beta, _ptr(cand_idx), _ptr(cand_cnt), _ptr(ws.buf),
         _stream()), "sa_update_score_tables")
 
 
@@ -341,6 +354,64 @@ def decode_step_append(prob: Problem, q, k_new, v_new, k_pool, v_pool, page_tabl
                                        _ptr(page_table), _ptr(seq_lens), _ptr(summaries), _ptr(sel_idx),
                                        _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(ws.buf), _stream()),
            "sa_decode_step_append")
+
+
+BYPASS_EPS = 0.85   # LFPS's sparsity threshold epsilon
+
+
+def kv_stats_shape(prob: Problem):
+    return (prob.B, prob.Hk, 3, prob.D)
+
+
+def kv_stats(prob: Problem, k_pool, v_pool, page_table, seq_lens, stats, ws: Workspace):
+    """Per (b, KV head) fp32 sums of k, k*k and v over the cached tokens (sa_kv_stats)."""
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool", tuple(k_pool.shape))
+    _need(page_table, torch.int32, "page_table", (prob.B, prob.max_pages_per_seq))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    _need(stats, torch.float32, "kv_stats", kv_stats_shape(prob))
+    _check(lib().sa_kv_stats(prob.ref, _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), _ptr(stats),
+                             _ptr(ws.buf), _stream()), "sa_kv_stats")
+
+
+def head_sparsity(prob: Problem, q, k_pool, page_table, seq_lens, stats, bypass, out, lse, ws: Workspace,
+                  eps: float = BYPASS_EPS, rho=None):
+    """LFPS's sink-share estimate per head and the mean-value bypass
+    (sa_head_sparsity): bypass[b][h] = rho > eps; bypassed rows of out / lse
+    receive the mean value row and the estimated log-normaliser."""
+    _need(q, torch.bfloat16, "q", (prob.B, prob.Hq, prob.D))
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(page_table, torch.int32, "page_table", (prob.B, prob.max_pages_per_seq))
+    _need(seq_lens, torch.int32, "seq_lens", (prob.B,))
+    _need(stats, torch.float32, "kv_stats", kv_stats_shape(prob))
+    _need(bypass, torch.int32, "bypass", (prob.B, prob.Hq))
+    _need(out, torch.float32, "out", (prob.B, prob.Hq, prob.D))
+    _need(lse, torch.float32, "lse", (prob.B, prob.Hq))
+    if rho is not None:
+        _need(rho, torch.float32, "rho", (prob.B, prob.Hq))
+    _check(lib().sa_head_sparsity(prob.ref, _ptr(q), _ptr(k_pool), _ptr(page_table), _ptr(seq_lens), _ptr(stats),
+                                  float(eps), _ptr(rho), _ptr(bypass), _ptr(out), _ptr(lse), _ptr(ws.buf),
+                                  _stream()), "sa_head_sparsity")
+
+
+def decode_step_bypass(prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, stats, sel_idx, sel_cnt,
+                       out, lse, bypass, ws: Workspace, eps: float = BYPASS_EPS, rho=None, k_new=None, v_new=None):
+    """The decode step with LFPS's head-sparsity bypass (sa_decode_step_bypass);
+    with k_new / v_new the new token is appended first and added to stats."""
+    _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse)
+    _need(stats, torch.float32, "kv_stats", kv_stats_shape(prob))
+    _need(bypass, torch.int32, "bypass", (prob.B, prob.Hq))
+    if rho is not None:
+        _need(rho, torch.float32, "rho", (prob.B, prob.Hq))
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+            _need(t, torch.bfloat16, nm, (prob.B, prob.Hk, prob.D))
+    _check(lib().sa_decode_step_bypass(prob.ref, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                       _ptr(page_table), _ptr(seq_lens), _ptr(summaries), _ptr(stats), float(eps),
+                                       _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(rho), _ptr(bypass),
+                                       _ptr(ws.buf), _stream()), "sa_decode_step_bypass")
 
 
 class DecodeStepCall:

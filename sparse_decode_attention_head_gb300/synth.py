@@ -20,9 +20,14 @@ describe; no public dataset is reproduced):
   ramp rising linearly from 0 to 1 (HGCA: recent entries dominate attention).
 * The page table is a seeded random permutation of physical pages, so the
   gather through it is a real scatter over the pool.
+* Sink-dominated heads (optional, the sparsity-bypass workloads): in each
+  sequence `sink_heads` query heads, drawn at random, get
+  q_h += c_qsink * k_0 / |k_0| with k_0 their KV head's key 0, so their
+  attention is held by the first token (LFPS measures about 12 % of heads
+  bypassed at epsilon = 0.85).
 
 Draw order (fixed, so a seed reproduces a case): group noise z_g, head noise
-z_h, K pool, V pool, page permutation, heavy-block picks.
+z_h, K pool, V pool, page permutation, heavy-block picks, sink-head picks.
 """
 from __future__ import annotations
 
@@ -59,6 +64,8 @@ class Workload:
     recency: int = 0                     # length of the recency ramp (0 = none)
     extra_tokens: int = 0                # page-table room for appended tokens
     lens: Optional[List[int]] = None     # per-sequence lengths (ragged batch); default all L
+    sink_heads: int = 0                  # query heads per sequence aligned with key 0
+    c_qsink: float = 24.0
 
     @property
     def G(self) -> int:
@@ -93,6 +100,13 @@ def workload(name: str) -> Workload:
         return Workload(name, B=16, Hq=28, Hk=4, L=65536, block_sizes=bs,
                         budget_bp=bp, S=4, W=1024, c_heavy=1.5, heavy_frac=0.01,
                         recency=2048)
+    if name == "tiny_4k_sinkheads":
+        # ragged: a long sequence, a short one, one with no global tokens, one token
+        return Workload(name, B=4, Hq=8, Hk=2, L=4096, block_sizes=[16, 16], budget_bp=[1000, 1000], S=4,
+                        W=256, c_sink=0.0, c_heavy=2.0, heavy_count=3, lens=[4096, 1000, 7, 1], sink_heads=2)
+    if name == "llama_32k_sinkheads":
+        return Workload(name, B=8, Hq=32, Hk=8, L=32768, block_sizes=[16] * 8, budget_bp=[500] * 8, S=4,
+                        W=1024, c_sink=0.0, c_heavy=1.5, heavy_frac=0.01, recency=2048, sink_heads=4)
     raise KeyError(name)
 
 
@@ -196,6 +210,18 @@ def make_decode_case(wl: Workload, seed: int, device="cpu") -> DecodeCase:
         blk = k_pool[rows]                                          # [npg, Hk, P, D]
         add = coef.reshape(Hk, npg, P).permute(1, 0, 2).unsqueeze(-1) * g_hat[b].reshape(1, Hk, 1, D)
         k_pool[rows] = blk + add
+
+    if wl.sink_heads > 0:
+        q = q.reshape(B, Hq, D).clone()
+        for b in range(B):
+            picks = torch.randperm(Hq, generator=g, device=dev)[:wl.sink_heads].tolist()
+            if lens[b] <= 0:
+                continue
+            row0 = int(page_table[b, 0])
+            for h in picks:
+                k0 = k_pool[row0, h // G, 0]
+                q[b, h] += wl.c_qsink * k0 / k0.norm()
+        q_bf = q.to(torch.bfloat16).contiguous()
 
     seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
     return DecodeCase(wl=wl, q=q_bf, k_pool=k_pool.to(torch.bfloat16),

@@ -141,6 +141,30 @@ def oracle_decode(nc: NpCase, wl: synth.Workload, sel: Dict[Tuple[int, int], np.
     return out
 
 
+def oracle_bypass(nc: NpCase, wl: synth.Workload, scale: float, units: Optional[List[Tuple[int, int]]] = None):
+    """{(b, h): (rho, lse_est, mean value row)} of the head-sparsity estimate."""
+    res = {}
+    units = units if units is not None else [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
+    for b, kvh in units:
+        kseq, vseq = oracle_kv(nc, b, kvh)
+        L = int(nc.seq_lens[b])
+        vbar = orc.bypass_output(vseq, L)
+        for g in range(wl.G):
+            h = kvh * wl.G + g
+            rho, lse = orc.head_sparsity(nc.q[b, h], kseq, L, scale)
+            res[(b, h)] = (rho, lse, vbar)
+    return res
+
+
+def oracle_kv_stats(nc: NpCase, b: int, kvh: int):
+    """fp64 sums of k, k*k and v over the sequence, and of |k|, k*k, |v| (the error scale)."""
+    kseq, vseq = oracle_kv(nc, b, kvh)
+    k, v = kseq.astype(np.float64), vseq.astype(np.float64)
+    sums = np.stack([k.sum(0), (k * k).sum(0), v.sum(0)])
+    mags = np.stack([np.abs(k).sum(0), (k * k).sum(0), np.abs(v).sum(0)])
+    return sums, mags
+
+
 # ------------------------------------------------------------------ GPU side
 
 def gpu_summaries(prob: sa.Problem, dev, ws):

@@ -52,7 +52,7 @@ def test_host_validation_before_launch(lib, kw, code):
     p = _prob(**kw)
     assert p.workspace_size() == 0
     vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
-    rc = lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, vp, None)
+    rc = lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, None, vp, None)
     assert rc == code
     rc = lib.sa_select_topk(p.ref, vp, vp, vp, vp, vp, None, vp, None)
     assert rc == code
@@ -63,8 +63,8 @@ def test_host_validation_before_launch(lib, kw, code):
 def test_null_pointers_rejected(lib):
     p = _prob()
     vp = ctypes.c_void_p(16)
-    assert lib.sa_sparse_decode(p.ref, None, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
-    assert lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 5, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_sparse_decode(p.ref, None, vp, vp, vp, vp, vp, vp, 0, vp, vp, None, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_sparse_decode(p.ref, vp, vp, vp, vp, vp, vp, vp, 5, vp, vp, None, None, vp, None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_score_blocks(p.ref, vp, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_block_summarize(p.ref, vp, vp, vp, -5, -1, vp, vp, None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_lse_merge(-1, 128, vp, vp, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
@@ -102,3 +102,25 @@ def test_group_selection_needs_one_budget_per_group():
     odd = sa.Problem(B=1, Hq=8, Hk=2, max_pages_per_seq=16, num_pages=16, sink=4, window=64, block_sizes=[16, 16],
                      k_per_head=[3] * 8, kcap=8, selection=7)
     assert sa.lib().sa_workspace_size(odd.ref) == 0
+
+
+def test_bypass_entries_validate_before_launch(lib):
+    p = _prob()
+    vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    # eps outside [0, 1], a missing flag array, missing stats
+    assert lib.sa_head_sparsity(p.ref, vp, vp, vp, vp, vp, 1.5, None, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_head_sparsity(p.ref, vp, vp, vp, vp, vp, -0.1, None, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_head_sparsity(p.ref, vp, vp, vp, vp, vp, 0.85, None, None, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_head_sparsity(p.ref, vp, vp, vp, vp, None, 0.85, None, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_kv_stats(p.ref, vp, vp, vp, vp, None, vp, None) == sa.SA_ERR_INVALID_ARG
+    step = lib.sa_decode_step_bypass
+    assert step(p.ref, vp, None, None, vp, vp, vp, vp, vp, None, 0.85, vp, vp, vp, vp, None, vp, vp, None) \
+        == sa.SA_ERR_INVALID_ARG                                            # no stats
+    assert step(p.ref, vp, None, None, vp, vp, vp, vp, vp, vp, 0.85, vp, vp, vp, vp, None, None, vp, None) \
+        == sa.SA_ERR_INVALID_ARG                                            # no flags
+    assert step(p.ref, vp, None, None, vp, vp, vp, vp, vp, vp, 2.0, vp, vp, vp, vp, None, vp, vp, None) \
+        == sa.SA_ERR_INVALID_ARG                                            # eps > 1
+    assert step(p.ref, vp, vp, None, vp, vp, vp, vp, vp, vp, 0.85, vp, vp, vp, vp, None, vp, vp, None) \
+        == sa.SA_ERR_INVALID_ARG                                            # k_new without v_new
+    bad = _prob(D=64)
+    assert lib.sa_kv_stats(bad.ref, vp, vp, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
