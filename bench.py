@@ -335,6 +335,7 @@ def run_ours(args):
     # end to end through the public binding: pinned host q in, O + lse out
     e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
     tables = None if args.no_tables else run_tables(args, dev)
+    bypass = None if args.no_bypass else run_bypass(args, dev, rank)
     gpu_launches = STEP_LAUNCHES * K
 
     res = {
@@ -365,6 +366,7 @@ def run_ours(args):
         "e2e": e2e,
         "tables_roofline": tables,
         "group_select_variant": group,
+        "bypass_variant": bypass,
         "gpu_launches": gpu_launches,
         "clocks": clk,
     }
@@ -565,6 +567,89 @@ def run_tables(args, dev, reps=100):
             "exact_token_topk": token_topk}
 
 
+def run_bypass(args, dev, rank, reps=200):
+    """The head-sparsity bypass (LFPS Algorithm 1 step 1, epsilon 0.85) on the
+    32K Llama shape with 4 of 32 query heads per sequence aligned with key 0
+    and no sink planted in the keys (llama_32k_sinkheads): sa_decode_step
+    against sa_decode_step_bypass on the same rotating layer copies, each a
+    CUDA graph of `reps` steps."""
+    wl = synth.workload("llama_32k_sinkheads")
+    ks = synth.k_per_qhead(wl)
+    kcap = max(ks)
+    prob = sa.Problem(B=wl.B, Hq=wl.Hq, Hk=wl.Hk, max_pages_per_seq=wl.max_pages_per_seq,
+                      num_pages=wl.B * wl.max_pages_per_seq, sink=wl.S, window=wl.W,
+                      block_sizes=wl.block_sizes, k_per_head=ks, kcap=kcap, mode=sa.SUMMARY_MINMAX)
+    ws = sa.Workspace(prob, device=dev)
+    layers = []
+    for l in range(N_LAYERS):
+        c = synth.make_decode_case(wl, 1000 * rank + 500 + l, device=dev)
+        summ = torch.empty(prob.summary_shape(), dtype=torch.bfloat16, device=dev)
+        sa.block_summarize(prob, c.k_pool, c.page_table, c.seq_lens, summ, ws)
+        st = torch.empty(sa.kv_stats_shape(prob), device=dev)
+        sa.kv_stats(prob, c.k_pool, c.v_pool, c.page_table, c.seq_lens, st, ws)
+        layers.append(dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens, summ=summ, st=st,
+                           sel_idx=torch.empty(wl.B, wl.Hq, kcap, dtype=torch.int32, device=dev),
+                           sel_cnt=torch.empty(wl.B, wl.Hq, dtype=torch.int32, device=dev),
+                           byp=torch.empty(wl.B, wl.Hq, dtype=torch.int32, device=dev)))
+        del c
+    out = torch.empty(wl.B, wl.Hq, wl.D, device=dev)
+    lse = torch.empty(wl.B, wl.Hq, device=dev)
+
+    def plain(L):
+        sa.decode_step(prob, L["q"], L["k"], L["v"], L["pt"], L["sl"], L["summ"], L["sel_idx"], L["sel_cnt"], out,
+                       lse, ws)
+
+    def bypass(L):
+        sa.decode_step_bypass(prob, L["q"], L["k"], L["v"], L["pt"], L["sl"], L["summ"], L["st"], L["sel_idx"],
+                              L["sel_cnt"], out, lse, L["byp"], ws)
+
+    stream = torch.cuda.Stream(device=dev)
+    res = {}
+    for name, fn in (("plain", plain), ("bypass", bypass)):
+        with torch.cuda.stream(stream):
+            for L in layers:
+                fn(L)
+        torch.cuda.synchronize()
+        if name == "bypass":
+            frac = float(np.mean([L["byp"].float().mean().item() for L in layers]))
+            nbytes = []
+            for L in layers:
+                nb = algorithmic_bytes(wl, prob, L["sl"].cpu().numpy(), L["sel_idx"], L["sel_cnt"])["total"]
+                # the estimate: sink + 6 window key rows and the sums per KV head, q per head,
+                # the mean row and lse per bypassed head
+                nb += wl.B * wl.Hk * (7 * wl.D * 2 + 3 * wl.D * 4) + wl.B * wl.Hq * (wl.D * 2 + 8)
+                nb += int(L["byp"].sum().item()) * (wl.D * 4 + 4)
+                nbytes.append(nb)
+        else:
+            nbytes = [algorithmic_bytes(wl, prob, L["sl"].cpu().numpy(), L["sel_idx"], L["sel_cnt"])["total"]
+                      for L in layers]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for i in range(reps):
+                    fn(layers[i % N_LAYERS])
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        b = float(np.mean([nbytes[i % N_LAYERS] for i in range(reps)]))
+        res[name] = {"ms_per_step": round(ms, 5), "value": round(wl.B * wl.Hq / (ms / 1e3), 1),
+                     "unit": "queries/s", "algorithmic_bytes_per_step": int(b),
+                     "achieved_gbs": round(b / (ms / 1e3) / 1e9, 1)}
+        del g
+    assert ws.status() == sa.SA_OK
+    return {"workload": "llama3.1-8b layer shape, ctx 32768, B8, 4 of 32 query heads per sequence "
+                        "sink-dominated (q aligned with key 0), no key sink; epsilon 0.85",
+            "bypassed_head_fraction": round(frac, 4),
+            "step_plain": res["plain"], "step_bypass": res["bypass"],
+            "speedup": round(res["plain"]["ms_per_step"] / res["bypass"]["ms_per_step"], 3)}
+
+
 # --------------------------------------------------------------------------- oracle timing
 
 def cpu_baseline(L, wl, ks, scale, budget_s=15.0, units=None):
@@ -636,6 +721,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-tables", action="store_true", help="skip the score-table (a7) leg")
     ap.add_argument("--no-group", action="store_true", help="skip the group-shared selection variant")
+    ap.add_argument("--no-bypass", action="store_true", help="skip the head-sparsity bypass variant")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -17,10 +17,11 @@
 // is the mean value row over the L tokens and its lse the log of the total.
 //
 // kv_stats_kernel builds the sums from the cache (one pass, fixed order);
-// sparsity_kernel optionally appends the new token's rows first (and adds
-// them to the sums), then estimates every query head of its KV head.
+// sparsity_kernel estimates every query head of a KV head with one warp
+// (estimate_unit_warp, which the decode step runs in a warp of its score
+// kernel).
 #include "sa_common.cuh"
-#include "summary.cuh"
+#include "sparsity.cuh"
 
 namespace sa {
 
@@ -102,148 +103,17 @@ int launch_kv_stats(const Params& p, const void* k_pool, const void* v_pool, con
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-constexpr int kLocalWindow = 6;
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// One CTA of 32 G threads per (KV head, sequence).  With k_new, warp 0 first
-// writes the new token's rows at L - 1 and adds them to the running sums; the
-// block barrier then makes them visible to every head's warp.  Rows written
-// here are read back with plain loads.
-__global__ void __launch_bounds__(32 * SA_MAX_GROUP)
-sparsity_kernel(Params p, const __nv_bfloat16* __restrict__ q, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
-                const int* __restrict__ page_table, const int* __restrict__ seq_lens,
-                const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new, float* stats,
-                float eps, float* __restrict__ rho_out, int* __restrict__ bypass, float* __restrict__ out,
-                float* __restrict__ lse, int* status) {
+// sa_head_sparsity: one warp per (KV head, sequence).
+__global__ void __launch_bounds__(32)
+sparsity_kernel(Params p, const __nv_bfloat16* __restrict__ q, const int* __restrict__ seq_lens, EstArgs E) {
   pdl_wait();
   pdl_trigger();
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int L = max(0, min(seq_lens[b], p.mpp * kP));
-  const int* pt = page_table + (size_t)b * p.mpp;
-  float* st = stats + ((size_t)b * p.Hk + kvh) * 3 * kD;
-  if (k_new != nullptr) {
-    if (warp == 0 && L > 0) {
-      append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, pt, status);
-      const size_t src = ((size_t)b * p.Hk + kvh) * kD;
-      const uint2 kr = reinterpret_cast<const uint2*>(k_new + src)[lane];
-      const uint2 vr = reinterpret_cast<const uint2*>(v_new + src)[lane];
-      const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
-      const float v4[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        st[4 * lane + i] += k4[i];
-        st[kD + 4 * lane + i] = __fmaf_rn(k4[i], k4[i], st[kD + 4 * lane + i]);
-        st[2 * kD + 4 * lane + i] += v4[i];
-      }
-    }
-    __syncthreads();
-  }
-  if (warp >= p.G) return;
-  const size_t row = (size_t)b * p.Hq + kvh * p.G + warp;
-  if (L == 0) {   // nothing to estimate: never bypassed
-    if (lane == 0) {
-      if (rho_out) rho_out[row] = 0.f;
-      bypass[row] = 0;
-    }
-    return;
-  }
-  float q4[4];
-  {
-    const uint2 qr = __ldg(reinterpret_cast<const uint2*>(q + row * kD) + lane);
-    q4[0] = bf16_lo(qr.x);
-    q4[1] = bf16_hi(qr.x);
-    q4[2] = bf16_lo(qr.y);
-    q4[3] = bf16_hi(qr.y);
-  }
-  const float scale = p.scale;
-  // the sink and the local window: their logits, and their key sums to take
-  // out of the running sums
-  const int lo = max(1, L - kLocalWindow);
-  float z[1 + kLocalWindow];
-  float ek[4] = {0.f, 0.f, 0.f, 0.f}, eq[4] = {0.f, 0.f, 0.f, 0.f};
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i <= kLocalWindow; ++i) {
-    const int t = i == 0 ? 0 : lo + i - 1;
-    z[i] = -INFINITY;
-    if (i > 0 && t >= L) continue;
-    const int phys = pt[t / kP];
-    if (phys < 0 || phys >= p.num_pages) {
-      bad = true;
-      continue;
-    }
-    const uint2 kr = reinterpret_cast<const uint2*>(k_pool + (((size_t)phys * p.Hk + kvh) * kP + t % kP) * kD)[lane];
-    const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
-    float d = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      d = __fmaf_rn(q4[c], k4[c], d);
-      ek[c] += k4[c];
-      eq[c] = __fmaf_rn(k4[c], k4[c], eq[c]);
-    }
-    z[i] = scale * warp_sum(d);
-  }
-  if (bad) {   // a broken page table: report, never bypass
-    if (lane == 0) {
-      set_status(status, SA_ERR_BAD_PAGE);
-      if (rho_out) rho_out[row] = 0.f;
-      bypass[row] = 0;
-    }
-    return;
-  }
-  const int n = lo - 1;   // global tokens [1, lo)
-  float zg = -INFINITY;
-  if (n > 0) {
-    const float inv_n = 1.0f / (float)n;
-    float qk = 0.f, qq = 0.f, var = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float kbar = (st[4 * lane + c] - ek[c]) * inv_n;
-      const float m2 = (st[kD + 4 * lane + c] - eq[c]) * inv_n;
-      qk = __fmaf_rn(q4[c], kbar, qk);
-      qq = __fmaf_rn(q4[c], q4[c], qq);
-      var += fmaxf(0.f, m2 - kbar * kbar);
-    }
-    qk = warp_sum(qk);
-    qq = warp_sum(qq);
-    var = warp_sum(var) * (1.0f / kD);
-    zg = logf((float)n) + scale * qk + 0.5f * scale * scale * qq * var;
-  }
-  float m = zg;
-#pragma unroll
-  for (int i = 0; i <= kLocalWindow; ++i) m = fmaxf(m, z[i]);
-  float tot = zg == -INFINITY ? 0.f : expf(zg - m);
-#pragma unroll
-  for (int i = 0; i <= kLocalWindow; ++i) tot += z[i] == -INFINITY ? 0.f : expf(z[i] - m);
-  const float rho = expf(z[0] - m) / tot;
-  const bool by = rho > eps;
-  if (lane == 0) {
-    if (rho_out) rho_out[row] = rho;
-    bypass[row] = by ? 1 : 0;
-  }
-  if (by) {
-    const float inv_l = 1.0f / (float)L;
-    const float4 o = make_float4(st[2 * kD + 4 * lane] * inv_l, st[2 * kD + 4 * lane + 1] * inv_l,
-                                 st[2 * kD + 4 * lane + 2] * inv_l, st[2 * kD + 4 * lane + 3] * inv_l);
-    *reinterpret_cast<float4*>(out + row * kD + 4 * lane) = o;
-    if (lane == 0) lse[row] = m + logf(tot);
-  }
+  estimate_unit_warp(p, E, q, seq_lens, blockIdx.y, blockIdx.x);
 }
 
-int launch_sparsity(const Params& p, const void* q, void* k_pool, void* v_pool, const int* page_table,
-                    const int* seq_lens, const void* k_new, const void* v_new, float* stats, float eps, float* rho,
-                    int* bypass, float* out, float* lse, int* status, cudaStream_t stream) {
-  const cudaError_t e = launch_pdl(
-      sparsity_kernel, dim3(p.Hk, p.B), dim3(32 * p.G), 0, stream, p, static_cast<const __nv_bfloat16*>(q),
-      static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool), page_table, seq_lens,
-      static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), stats, eps, rho, bypass,
-      out, lse, status);
+int launch_sparsity(const Params& p, const void* q, const int* seq_lens, const EstArgs& E, cudaStream_t stream) {
+  const cudaError_t e = launch_pdl(sparsity_kernel, dim3(p.Hk, p.B), dim3(32), 0, stream, p,
+                                   static_cast<const __nv_bfloat16*>(q), seq_lens, E);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -71,9 +71,10 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
   const int win = min(p.mpp, kWinPages);
   const int kvh = blockIdx.x, b = blockIdx.y;
   const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
+  const uint32_t active = unit_active_heads(p, b, kvh);
   build_unit_tiles<kBuildThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0, gran, tiles,
                                   ntiles, out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win),
-                                  scan_tmp);
+                                  scan_tmp, active);
 }
 
 // ------------------------------------------------------------------ decode
@@ -160,6 +161,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   int* s_misc = reinterpret_cast<int*>(s_empty + nslots);                    // 32 ints
   int* s_prefix = s_misc + 32;                                               // U + 1: tiles before unit u
   int* s_cprefix = s_prefix + U + 1;                                         // U + 1: chunks before unit u
+  uint8_t* s_umask = reinterpret_cast<uint8_t*>(s_cprefix + U + 1);         // U bytes: heads left out (bypass)
   // s_misc: [17] chunks published, [18] chunks combined, [19] chunks fully
   // issued, [20] consumer warps parked on the current chunk
 
@@ -182,7 +184,14 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   const int a = min(U, tid * per), e = min(U, a + per);
   {
     int cnt = 0;
-    for (int i = a; i < e; ++i) cnt += A.ntiles[i];
+    for (int i = a; i < e; ++i) {
+      cnt += A.ntiles[i];
+      if (p.bypass != nullptr) {   // heads answered by the sparsity bypass: their rows are not written
+        int m = 0;
+        for (int g = 0; g < G; ++g) m |= (p.bypass[(size_t)i * G + g] != 0 ? 1 : 0) << g;
+        s_umask[i] = (uint8_t)m;
+      }
+    }
     int x = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -617,7 +626,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       }
       if (whole) {
         const size_t row = (size_t)b * p.Hq + kvh * G + g;
-        if (p.bypass != nullptr && p.bypass[row]) continue;
+        if (p.bypass != nullptr && ((s_umask[u] >> g) & 1)) continue;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         *reinterpret_cast<float4*>(A.out + row * kD + 4 * lane) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -699,7 +708,7 @@ size_t decode_smem_bytes_n(int U, int G, int nslots) {
   return 1024 + (size_t)nslots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * G * kPart * 4 +
          nslots * sizeof(SlotInfo) + kChunkRing * sizeof(ChunkInfo) + kChunkRing * kConsWarps * 4 +
          2 * nslots * 8 + 32 * 4 +
-         2 * (size_t)(U + 1) * 4;
+         (2 * (size_t)(U + 1) + (U + 3) / 4) * 4;
 }
 
 // Slot count: the largest multiple of kConsWarps (<= 16) that still lets two

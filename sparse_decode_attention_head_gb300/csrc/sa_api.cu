@@ -10,13 +10,14 @@
 #include <mutex>
 
 #include "sa_common.cuh"
+#include "sparsity.cuh"
 #include "tables.cuh"
 
 namespace sa {
 int launch_summarize(const Params& p, const void* k_pool, const int* page_table, const int* seq_lens,
                      int block_begin, int block_end, void* summ, int* status, cudaStream_t stream);
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
-                 int always, int num_sms, cudaStream_t stream);
+                 int always, int num_sms, cudaStream_t stream, const EstArgs* est);
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream);
 size_t topk_smem_bytes(const Params& p);
@@ -32,7 +33,7 @@ size_t tiles_bytes(const Params& p);
 int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                      const float* lse_b, float* o, float* lse, cudaStream_t stream);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
-                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, int* sel_cnt,
+                      const void* k_new, const void* v_new, float* stats, void* summ, const int* sel_idx, int* sel_cnt,
                       void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                       cudaStream_t stream);
 int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table, const void* k_new, const void* v_new,
@@ -41,14 +42,12 @@ int launch_token_topk(const Params& p, const void* q, const void* k_pool, const 
                       const int* cand_idx, const int* cand_cnt, int* sel_idx, int* sel_cnt, float* scores_out,
                       int* status, cudaStream_t stream);
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
-                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, void* summ, int* sel_idx,
-                        int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
-                        cudaStream_t stream);
+                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, float* stats, void* summ,
+                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status,
+                        int* ticket, cudaStream_t stream);
 int launch_kv_stats(const Params& p, const void* k_pool, const void* v_pool, const int* page_table,
                     const int* seq_lens, float* stats, int* status, cudaStream_t stream);
-int launch_sparsity(const Params& p, const void* q, void* k_pool, void* v_pool, const int* page_table,
-                    const int* seq_lens, const void* k_new, const void* v_new, float* stats, float eps, float* rho,
-                    int* bypass, float* out, float* lse, int* status, cudaStream_t stream);
+int launch_sparsity(const Params& p, const void* q, const int* seq_lens, const EstArgs& E, cudaStream_t stream);
 }  // namespace sa
 
 using sa::Params;
@@ -284,7 +283,7 @@ int sa_score_blocks(const sa_problem* prob, const void* q, const void* summaries
   if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
   const int nsm = num_sms_current();
   if (nsm <= 0) return SA_ERR_CUDA;
-  return sa::launch_score(p, q, summaries, seq_lens, scores, 1, nsm, as_stream(stream));
+  return sa::launch_score(p, q, summaries, seq_lens, scores, 1, nsm, as_stream(stream), nullptr);
 }
 
 int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries, const int32_t* seq_lens,
@@ -300,7 +299,7 @@ int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries,
   cudaStream_t s = as_stream(stream);
   const int nsm = num_sms_current();
   if (nsm <= 0) return SA_ERR_CUDA;
-  rc = sa::launch_score(p, q, summaries, seq_lens, scores, scores_or_null != nullptr, nsm, s);
+  rc = sa::launch_score(p, q, summaries, seq_lens, scores, scores_or_null != nullptr, nsm, s, nullptr);
   if (rc != SA_OK) return rc;
   return sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s);
 }
@@ -369,22 +368,26 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   float* scores = at<float>(ws, l.scores);
   void* kp = const_cast<void*>(k_pool);
   void* vp = const_cast<void*>(v_pool);
+  // the head-sparsity estimate runs in the score kernel's first warps; it
+  // takes the new token's rows from k_new / v_new (the append, and their
+  // addition to the sums, follow in the tile-building kernel)
+  sa::EstArgs E{};
   if (kv_stats != nullptr) {
-    rc = sa::launch_sparsity(p, q, kp, vp, page_table, seq_lens, k_new, v_new, kv_stats, eps, rho, bypass, out, lse,
-                             status, s);
-    if (rc != SA_OK) return rc;
-    p.bypass = bypass;
-    k_new = v_new = nullptr;   // appended above
+    E = sa::EstArgs{static_cast<const __nv_bfloat16*>(k_pool), page_table,
+                    static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), kv_stats,
+                    eps, rho, bypass, out, lse, status};
   }
   // the scores never read the newest token's block (it is in the window), so
   // the append and the tail summary can follow them
-  if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s)) != SA_OK) return rc;
+  if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s, kv_stats ? &E : nullptr)) != SA_OK)
+    return rc;
+  if (kv_stats != nullptr) p.bypass = bypass;
   int* ticket = at<int>(ws, l.counters) + p.B * p.Hk + 1;
-  rc = sa::launch_select_build(p, scores, seq_lens, page_table, kp, vp, k_new, v_new, summaries, sel_idx, sel_cnt,
-                               at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+  rc = sa::launch_select_build(p, scores, seq_lens, page_table, kp, vp, k_new, v_new, kv_stats, summaries, sel_idx,
+                               sel_cnt, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
   if (rc == SA_ERR_UNSUPPORTED) {   // candidates beyond the fused kernel's capacity: two kernels
     if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
-    rc = sa::launch_build_step(p, seq_lens, page_table, kp, vp, k_new, v_new, summaries, sel_idx, sel_cnt,
+    rc = sa::launch_build_step(p, seq_lens, page_table, kp, vp, k_new, v_new, kv_stats, summaries, sel_idx, sel_cnt,
                                at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
   }
   if (rc != SA_OK) return rc;
@@ -444,10 +447,10 @@ int sa_head_sparsity(const sa_problem* prob, const void* q, const void* k_pool, 
   if (!(eps >= 0.f && eps <= 1.f)) return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(kv_stats) || !aligned16(out)) return SA_ERR_INVALID_ARG;
   const Layout l = layout_of(p);
-  // without k_new the kernel neither writes the pools nor the sums
-  return sa::launch_sparsity(p, q, const_cast<void*>(k_pool), nullptr, page_table, seq_lens, nullptr, nullptr,
-                             const_cast<float*>(kv_stats), eps, rho_or_null, bypass, out, lse,
-                             at<int>(ws, l.header), as_stream(stream));
+  // without k_new the estimate reads the sums and writes nothing back
+  const sa::EstArgs E{static_cast<const __nv_bfloat16*>(k_pool), page_table, nullptr, nullptr,
+                      const_cast<float*>(kv_stats), eps, rho_or_null, bypass, out, lse, at<int>(ws, l.header)};
+  return sa::launch_sparsity(p, q, seq_lens, E, as_stream(stream));
 }
 
 int sa_append_kv(const sa_problem* prob, const void* k_new, const void* v_new, void* k_pool, void* v_pool,

@@ -17,11 +17,15 @@
 #include <algorithm>
 
 #include "sa_common.cuh"
+#include "sparsity.cuh"
 #include "topk.cuh"
 
 namespace sa {
 
 constexpr int kScoreWarps = 15;                // consumer warps (+1 producer warp: 4 warps per scheduler)
+// threads of a CTA: the consumers, the producer, and with EST the warp of the
+// head-sparsity estimate
+constexpr int score_threads(bool est) { return (kScoreWarps + (est ? 2 : 1)) * 32; }
 constexpr int kMaxUnitsScore = 4096;
 
 // Work items are (unit = (b, kv head), run of kItemBlocks candidate blocks).
@@ -29,7 +33,9 @@ constexpr int kMaxUnitsScore = 4096;
 // item's summaries (contiguous) and the group's q into a ring of shared-memory
 // stages with 1-D bulk copies, and leaves a descriptor of the item (where its
 // scores go, how many blocks it holds) beside the stage; consumer warps score
-// the staged blocks.
+// the staged blocks.  With EST a last warp runs the head-sparsity estimate of
+// units blockIdx.x, blockIdx.x + gridDim.x, ... beside them (its own
+// instantiation: the extra warp lowers the register cap).
 struct ItemDesc {
   long long sbase;   // scores index of (b, first head of the group, first block of the item)
   int nb;            // blocks in the item
@@ -58,10 +64,10 @@ constexpr int item_blocks(int G) {
        : G == 7 ? ScoreShape<7>::kItemBlocks : ScoreShape<8>::kItemBlocks;
 }
 
-template <int G, int MODE>
-__global__ void __launch_bounds__((kScoreWarps + 1) * 32, 1)
+template <int G, int MODE, bool EST>
+__global__ void __launch_bounds__(score_threads(EST), 1)
 score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ summ,
-             const int* __restrict__ seq_lens, float* __restrict__ scores, int always, int nstages) {
+             const int* __restrict__ seq_lens, float* __restrict__ scores, int always, int nstages, EstArgs E) {
   pdl_wait();
   pdl_trigger();
   constexpr int kRowElems = (MODE == SA_SUMMARY_MINMAX) ? 2 * kD : kD;
@@ -108,6 +114,10 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   const long long total = s_items[U];
   const long long it_lo = total * blockIdx.x / gridDim.x, it_hi = total * (blockIdx.x + 1) / gridDim.x;
   const int n_items = (int)(it_hi - it_lo);
+  if (EST && warp == kScoreWarps + 1) {   // ---------------- head-sparsity estimate
+    for (int u = blockIdx.x; u < U; u += gridDim.x) estimate_unit_warp(p, E, q, seq_lens, u / p.Hk, u % p.Hk);
+    return;
+  }
   if (n_items <= 0) return;
 
   if (warp == kScoreWarps) {   // ---------------- producer
@@ -286,8 +296,11 @@ topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ 
 }
 
 int launch_score(const Params& p, const void* q, const void* summ, const int* seq_lens, float* scores,
-                 int always, int num_sms, cudaStream_t stream) {
+                 int always, int num_sms, cudaStream_t stream, const EstArgs* est_args) {
   if (p.B * p.Hk > kMaxUnitsScore) return SA_ERR_UNSUPPORTED;
+  EstArgs E{};
+  if (est_args != nullptr) E = *est_args;
+  const bool est = E.stats != nullptr;
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* sb = static_cast<const __nv_bfloat16*>(summ);
   const int row_bytes = (p.mode == SA_SUMMARY_MINMAX ? 2 : 1) * kD * 2;
@@ -296,19 +309,23 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
   const size_t smem = stage * nstages;
   const int grid = std::max(1, num_sms);
   cudaError_t err = cudaSuccess;
-#define SA_SCORE_CASE(GG)                                                                         \
-  case GG:                                                                                        \
-    if (p.mode == SA_SUMMARY_MINMAX) {                                                            \
-      smem_limit_at_least(reinterpret_cast<const void*>(score_kernel<GG, SA_SUMMARY_MINMAX>),     \
-                          (int)smem);                                                             \
-      err = launch_pdl(score_kernel<GG, SA_SUMMARY_MINMAX>, dim3(grid), dim3((kScoreWarps + 1) * 32), \
-                       smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
-    } else {                                                                                      \
-      smem_limit_at_least(reinterpret_cast<const void*>(score_kernel<GG, SA_SUMMARY_MEAN>),       \
-                          (int)smem);                                                             \
-      err = launch_pdl(score_kernel<GG, SA_SUMMARY_MEAN>, dim3(grid), dim3((kScoreWarps + 1) * 32),   \
-                       smem, stream, p, qb, sb, seq_lens, scores, always, nstages);               \
-    }                                                                                             \
+#define SA_SCORE_LAUNCH(GG, MM, EE)                                                       \
+  smem_limit_at_least(reinterpret_cast<const void*>(score_kernel<GG, MM, EE>), (int)smem); \
+  err = launch_pdl(score_kernel<GG, MM, EE>, dim3(grid), dim3(score_threads(EE)), smem,    \
+                   stream, p, qb, sb, seq_lens, scores, always, nstages, E);
+#define SA_SCORE_CASE(GG)                                  \
+  case GG:                                                 \
+    if (p.mode == SA_SUMMARY_MINMAX) {                     \
+      if (est) {                                           \
+        SA_SCORE_LAUNCH(GG, SA_SUMMARY_MINMAX, true)       \
+      } else {                                             \
+        SA_SCORE_LAUNCH(GG, SA_SUMMARY_MINMAX, false)      \
+      }                                                    \
+    } else if (est) {                                      \
+      SA_SCORE_LAUNCH(GG, SA_SUMMARY_MEAN, true)           \
+    } else {                                               \
+      SA_SCORE_LAUNCH(GG, SA_SUMMARY_MEAN, false)          \
+    }                                                      \
     break;
   switch (p.G) {
     SA_SCORE_CASE(1)
@@ -322,6 +339,7 @@ int launch_score(const Params& p, const void* q, const void* summ, const int* se
     default:
       return SA_ERR_UNSUPPORTED;
   }
+#undef SA_SCORE_LAUNCH
 #undef SA_SCORE_CASE
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }

@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "sa_common.cuh"
+#include "sparsity.cuh"
 #include "summary.cuh"
 #include "tiles.cuh"
 #include "topk.cuh"
@@ -26,9 +27,9 @@ constexpr int kStepTileThreads = kStepBuildThreads - 32;
 __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                   __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const __nv_bfloat16* __restrict__ k_new,
-                  const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ summ, const int* sel_idx,
-                  int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
-                  float* __restrict__ lse, int* status, int* ticket) {
+                  const __nv_bfloat16* __restrict__ v_new, float* stats, __nv_bfloat16* __restrict__ summ,
+                  const int* sel_idx, int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles,
+                  float* __restrict__ out, float* __restrict__ lse, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
@@ -37,24 +38,27 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
   const int kvh = blockIdx.x, b = blockIdx.y;
   if (threadIdx.x >= kStepTileThreads) {
     const int L = min(seq_lens[b], p.mpp * kP);
-    if (k_new != nullptr)
+    if (k_new != nullptr) {
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
+      if (stats != nullptr) stats_add_new_warp(p, stats, k_new, v_new, b, kvh, L);   // read by the scores only
+    }
     if (L > 0)
       summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
     return;
   }
   const int win = min(p.mpp, kWinPages);
   const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
+  const uint32_t active = unit_active_heads(p, b, kvh);
   build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0,
                                      SA_SEL_BLOCK, tiles, ntiles, out, lse, status, smem_b,
-                                     reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
+                                     reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active);
   // the builder's reads of the counts ended at its last barrier: heads
   // answered by the sparsity bypass report no selection
   if (p.bypass != nullptr && threadIdx.x < p.G && p.bypass[h0 + threadIdx.x]) sel_cnt[h0 + threadIdx.x] = 0;
 }
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
-                      const void* k_new, const void* v_new, void* summ, const int* sel_idx, int* sel_cnt,
+                      const void* k_new, const void* v_new, float* stats, void* summ, const int* sel_idx, int* sel_cnt,
                       void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                       cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
@@ -63,7 +67,7 @@ int launch_build_step(const Params& p, const int* seq_lens, const int* page_tabl
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
                                    seq_lens, page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
-                                   static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(summ),
+                                   static_cast<const __nv_bfloat16*>(v_new), stats, static_cast<__nv_bfloat16*>(summ),
                                    sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
@@ -102,7 +106,7 @@ template <int GROUP, int KPT>
 __global__ void __launch_bounds__(kStepBuildThreads)
 select_build_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
                     const int* __restrict__ page_table, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
-                    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new, float* stats,
                     __nv_bfloat16* __restrict__ summ, int* __restrict__ sel_idx, int* __restrict__ sel_cnt,
                     Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
                     float* __restrict__ lse, int* status, int* ticket) {
@@ -118,6 +122,7 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   int* s_sel = smem_b + 5 * win;
   int* s_cnt = s_sel + G * p.kcap;
   const int L = min(seq_lens[b], p.mpp * kP);
+  const uint32_t active = unit_active_heads(p, b, kvh);   // loaded now, used after the top-k
   int j0, j1;
   candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
   const int g = tid / GROUP;
@@ -135,35 +140,40 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   }
   __syncthreads();
   const size_t h0 = (size_t)b * p.Hq + kvh * G;
-  // heads answered by the sparsity bypass select nothing (the builder skips them)
-  auto bypassed = [&](int gg) { return p.bypass != nullptr && p.bypass[h0 + gg] != 0; };
+  if (p.bypass != nullptr) {   // heads answered by the sparsity bypass select nothing
+    if (tid < G && !((active >> tid) & 1u)) s_cnt[tid] = 0;
+    __syncthreads();
+  }
   for (int i = tid; i < G * p.kcap; i += kStepBuildThreads)
-    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap] && !bypassed(i / p.kcap)) sel_idx[h0 * p.kcap + i] = s_sel[i];
-  if (tid < G) sel_cnt[h0 + tid] = bypassed(tid) ? 0 : s_cnt[tid];
+    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
+  if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
   if (tid >= kStepTileThreads) {
-    if (k_new != nullptr)
+    if (k_new != nullptr) {
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
+      if (stats != nullptr) stats_add_new_warp(p, stats, k_new, v_new, b, kvh, L);   // read by the scores only
+    }
     if (L > 0)
       summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
     return;
   }
   build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, s_sel, s_cnt, SA_SEL_BLOCK, tiles, ntiles, out,
-                                     lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp);
+                                     lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active);
 }
 
 // SA_ERR_UNSUPPORTED when some head's candidates exceed the fused kernel's
 // key capacity or its shared memory would not fit; the caller then runs
 // topk_kernel + build_step_kernel.
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
-                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, void* summ, int* sel_idx,
-                        int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
-                        cudaStream_t stream) {
+                        void* k_pool, void* v_pool, const void* k_new, const void* v_new, float* stats, void* summ,
+                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status,
+                        int* ticket, cudaStream_t stream) {
   int max_n = 0;
   for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
   const size_t smem = build_smem_bytes(p.mpp) + ((size_t)p.G * p.kcap + p.G) * sizeof(int);
   if (smem > 160 * 1024) return SA_ERR_UNSUPPORTED;
   void (*kern)(Params, const float*, const int*, const int*, __nv_bfloat16*, __nv_bfloat16*, const __nv_bfloat16*,
-               const __nv_bfloat16*, __nv_bfloat16*, int*, int*, Tile*, int*, float*, float*, int*, int*) = nullptr;
+               const __nv_bfloat16*, float*, __nv_bfloat16*, int*, int*, Tile*, int*, float*, float*, int*,
+               int*) = nullptr;
   if (p.G <= 4) {
     if (max_n <= 256 * 8) kern = select_build_kernel<256, 8>;
     else if (max_n <= 256 * 16) kern = select_build_kernel<256, 16>;
@@ -175,7 +185,7 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
   const cudaError_t e = launch_pdl(kern, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p, scores, seq_lens,
                                    page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
-                                   static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(summ),
+                                   static_cast<const __nv_bfloat16*>(v_new), stats, static_cast<__nv_bfloat16*>(summ),
                                    sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }

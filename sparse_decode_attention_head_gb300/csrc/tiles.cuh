@@ -27,6 +27,16 @@ __device__ __forceinline__ void item_range(int gran, int x, int Bs, int Lc, int 
   }
 }
 
+// G-bit mask of the unit's heads that attend: those not answered by the
+// sparsity bypass (all heads when p.bypass is NULL).
+__device__ __forceinline__ uint32_t unit_active_heads(const Params& p, int b, int kvh) {
+  uint32_t active = (1u << p.G) - 1u;
+  if (p.bypass != nullptr)
+    for (int g = 0; g < p.G; ++g)
+      if (p.bypass[(size_t)b * p.Hq + kvh * p.G + g]) active &= ~(1u << g);
+  return active;
+}
+
 // Pages per builder window: the builder keeps a flag and 16 token masks per
 // page of the current window in shared memory (20 bytes a page).
 constexpr int kWinPages = 4096;
@@ -43,8 +53,9 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
 // then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
 // a block scan of the page flags, and one 32-byte store per tile.
 // sel_row: the unit's selections [G][kcap] (global or shared memory),
-// cnt_row: their counts [G].  Heads flagged in p.bypass are left out: no
-// tokens attend for them and their output rows are not written.  s_flag: window ints, s_mask: 4 window words,
+// cnt_row: their counts [G].  active: the heads that attend (G bits); the
+// others are left out -- no tokens attend for them and their output rows are
+// not written.  s_flag: window ints, s_mask: 4 window words,
 // scan_tmp: 32 ints.
 template <int NT>
 __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh, const int* __restrict__ seq_lens,
@@ -52,7 +63,7 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
                                                  const int* cnt_row, int gran, Tile* __restrict__ tiles,
                                                  int* __restrict__ ntiles, float* __restrict__ out,
                                                  float* __restrict__ lse, int* status, int* s_flag, uint32_t* s_mask,
-                                                 int* scan_tmp) {
+                                                 int* scan_tmp, uint32_t active) {
   constexpr int kPer = (kWinPages + NT - 1) / NT;   // pages per thread and window, at most
   constexpr int kItemRegs = 2;                      // selection entries prefetched per thread (r = 0, 1 below)
   auto bsync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); };
@@ -64,10 +75,6 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   const int per = (win + NT - 1) / NT;
   // ---- up-front loads
   const int Lraw = seq_lens[b];
-  uint32_t active = (1u << p.G) - 1u;   // heads whose rows this unit writes
-  if (p.bypass != nullptr)
-    for (int g = 0; g < p.G; ++g)
-      if (p.bypass[(size_t)b * p.Hq + kvh * p.G + g]) active &= ~(1u << g);
   int ptr[kPer];
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
