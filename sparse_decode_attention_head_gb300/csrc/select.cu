@@ -265,7 +265,8 @@ score_kernel(Params p, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 
 // ---------------------------------------------------------------- top-k
 
-template <int NT, int KPT>
+// GRP: group-shared selection, its own instantiation (see select_build_kernel).
+template <int NT, int KPT, bool GRP>
 __global__ void __launch_bounds__(NT)
 topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
             int* __restrict__ sel_idx, int* __restrict__ sel_cnt) {
@@ -275,12 +276,12 @@ topk_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ 
   const int b = blockIdx.y;
   const int L = min(seq_lens[b], p.mpp * kP);
   int j0, j1;
-  if (p.sel_mode == SA_SELECT_GROUP) {   // one CTA per KV head: the group's summed scores, one list for all
+  if (GRP) {   // one CTA per KV head: the group's summed scores, one list for all
     const int kvh = blockIdx.x, h0 = kvh * p.G;
     candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
     int* row0 = sel_idx + ((size_t)b * p.Hq + h0) * p.kcap;
-    group_topk<NT, KPT>(scores + ((size_t)b * p.Hq + h0) * p.slots + j0, j1 - j0, p.k[h0], j0, row0,
-                        sel_cnt + (size_t)b * p.Hq + h0, 0, S, p.G, (size_t)p.slots);
+    group_topk<NT, KPT, true>(scores + ((size_t)b * p.Hq + h0) * p.slots + j0, j1 - j0, p.k[h0], j0, row0,
+                              sel_cnt + (size_t)b * p.Hq + h0, 0, S, p.G, (size_t)p.slots);
     __syncthreads();
     const int cnt = sel_cnt[(size_t)b * p.Hq + h0];
     for (int g = 1; g < p.G; ++g) {
@@ -352,13 +353,17 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
   // the largest candidate count any head can have
   int max_n = 0;
   for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  const bool grp = p.sel_mode == SA_SELECT_GROUP;
   cudaError_t e;
   if (max_n <= 256 * 8)
-    e = launch_pdl(topk_kernel<256, 8>, grid, dim3(256), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(grp ? topk_kernel<256, 8, true> : topk_kernel<256, 8, false>, grid, dim3(256), 0, stream, p,
+                   scores, seq_lens, sel_idx, sel_cnt);
   else if (max_n <= 1024 * 16)
-    e = launch_pdl(topk_kernel<1024, 16>, grid, dim3(1024), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(grp ? topk_kernel<1024, 16, true> : topk_kernel<1024, 16, false>, grid, dim3(1024), 0, stream, p,
+                   scores, seq_lens, sel_idx, sel_cnt);
   else if (max_n <= 1024 * 64)
-    e = launch_pdl(topk_kernel<1024, 64>, grid, dim3(1024), 0, stream, p, scores, seq_lens, sel_idx, sel_cnt);
+    e = launch_pdl(grp ? topk_kernel<1024, 64, true> : topk_kernel<1024, 64, false>, grid, dim3(1024), 0, stream, p,
+                   scores, seq_lens, sel_idx, sel_cnt);
   else
     return SA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;

@@ -101,8 +101,10 @@ int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table
 // selections kept in shared memory), then the tile list of their union
 // (warps 0..30) and the tail summary (warp 31), as build_step_kernel.  It
 // replaces topk_kernel + build_step_kernel when every head's candidates fit
-// GROUP x KPT keys.
-template <int GROUP, int KPT>
+// GROUP x KPT keys.  GRP (group-shared selection) and APPEND (the new
+// token's rows written too) are separate instantiations, so that the plain
+// step's kernel carries none of their code or registers.
+template <int GROUP, int KPT, bool GRP, bool APPEND>
 __global__ void __launch_bounds__(kStepBuildThreads)
 select_build_kernel(Params p, const float* __restrict__ scores, const int* __restrict__ seq_lens,
                     const int* __restrict__ page_table, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
@@ -126,10 +128,10 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   int j0, j1;
   candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
   const int g = tid / GROUP;
-  if (p.sel_mode == SA_SELECT_GROUP) {   // one list for the group, from the summed scores
+  if (GRP) {   // one list for the group, from the summed scores
     if (g == 0)
-      group_topk<GROUP, KPT>(scores + ((size_t)b * p.Hq + kvh * G) * p.slots + j0, j1 - j0, p.k[kvh * G], j0,
-                             s_sel, s_cnt, 1, S[0], G, (size_t)p.slots);
+      group_topk<GROUP, KPT, true>(scores + ((size_t)b * p.Hq + kvh * G) * p.slots + j0, j1 - j0, p.k[kvh * G], j0,
+                                   s_sel, s_cnt, 1, S[0], G, (size_t)p.slots);
     __syncthreads();
     for (int i = tid; i < (G - 1) * p.kcap; i += kStepBuildThreads) s_sel[p.kcap + i] = s_sel[i % p.kcap];
     if (tid > 0 && tid < G) s_cnt[tid] = s_cnt[0];
@@ -148,7 +150,7 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
     if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
   if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
   if (tid >= kStepTileThreads) {
-    if (k_new != nullptr) {
+    if (APPEND) {
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
       if (stats != nullptr) stats_add_new_warp(p, stats, k_new, v_new, b, kvh, L);   // read by the scores only
     }
@@ -174,12 +176,17 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
   void (*kern)(Params, const float*, const int*, const int*, __nv_bfloat16*, __nv_bfloat16*, const __nv_bfloat16*,
                const __nv_bfloat16*, float*, __nv_bfloat16*, int*, int*, Tile*, int*, float*, float*, int*,
                int*) = nullptr;
+  const int v = (p.sel_mode == SA_SELECT_GROUP ? 2 : 0) | (k_new != nullptr ? 1 : 0);
+#define SA_SB_PICK(GG, KK)                                                             \
+  (v == 0 ? select_build_kernel<GG, KK, false, false> : v == 1 ? select_build_kernel<GG, KK, false, true> \
+   : v == 2 ? select_build_kernel<GG, KK, true, false> : select_build_kernel<GG, KK, true, true>)
   if (p.G <= 4) {
-    if (max_n <= 256 * 8) kern = select_build_kernel<256, 8>;
-    else if (max_n <= 256 * 16) kern = select_build_kernel<256, 16>;
+    if (max_n <= 256 * 8) kern = SA_SB_PICK(256, 8);
+    else if (max_n <= 256 * 16) kern = SA_SB_PICK(256, 16);
   } else {
-    if (max_n <= 128 * 16) kern = select_build_kernel<128, 16>;
+    if (max_n <= 128 * 16) kern = SA_SB_PICK(128, 16);
   }
+#undef SA_SB_PICK
   if (kern == nullptr) return SA_ERR_UNSUPPORTED;
   if (smem > 48 * 1024) smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
   const cudaError_t e = launch_pdl(kern, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p, scores, seq_lens,

@@ -46,10 +46,12 @@ __device__ __forceinline__ int group_excl_scan(int v, int* tmp, int bar_id) {
 }
 
 // Group-collective.  sc: the head's candidate scores (n of them, block ids
-// base_idx + i); with nrows > 1 the key of block i is the fp32 sum, in row
-// order, of sc[r * row_stride + i] over the rows (a selection shared by a
-// KV head's query heads).  k_req: blocks to keep.  Writes out[0..) and *cnt_out.
-template <int GROUP, int KPT>
+// base_idx + i); with ROWS the key of block i is the fp32 sum, in row order,
+// of sc[r * row_stride + i] over nrows rows (a selection shared by a KV
+// head's query heads) -- a separate instantiation, so that the one-row case
+// keeps its loads independent of each other.  k_req: blocks to keep.  Writes
+// out[0..) and *cnt_out.
+template <int GROUP, int KPT, bool ROWS = false>
 __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int base_idx, int* __restrict__ out,
                            int* __restrict__ cnt_out, int bar_id, TopkScratch& S, int nrows = 1,
                            size_t row_stride = 0) {
@@ -69,7 +71,8 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
     float x = 0.f;
     if (i < n) {
       x = sc[i];
-      for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, sc[r * row_stride + i]);
+      if (ROWS)
+        for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, sc[r * row_stride + i]);
     }
     key[q] = i < n ? order_key(x) : 0u;
     if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
