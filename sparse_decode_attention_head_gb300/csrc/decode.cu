@@ -140,6 +140,9 @@ __device__ __forceinline__ void st_release_cta(int* x, int v) {
   asm volatile("st.release.cta.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
 }
 
+// LOGITS: the instantiation that also writes every attended logit (A.logits,
+// for the score tables); the plain decode carries none of that code.
+template <bool LOGITS>
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, int nslots) {
@@ -511,7 +514,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
           for (int mt = 0; mt < 8; ++mt) {
             o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
           }
-          if (A.logits != nullptr) {
+          if (LOGITS) {
             const int base_tok = info->lp * kP;
             const size_t hs = (size_t)p.mpp * kP;
             const size_t row0 = ((size_t)b * p.Hq + kvh * G) * hs;
@@ -751,8 +754,10 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   const int nslots = decode_slots(U, p.G);
   const size_t smem = decode_smem_bytes_n(U, p.G, nslots);
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
-  smem_limit_at_least(reinterpret_cast<const void*>(decode_kernel), (int)smem);
-  const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(decode_kernel), kDecThreads, smem);
+  void (*kern)(Params, DecodeArgs, const CUtensorMap, const CUtensorMap, int) =
+      logits != nullptr ? decode_kernel<true> : decode_kernel<false>;
+  smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
+  const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(kern), kDecThreads, smem);
   const int grid = std::min(kMaxCtas, num_sms * per_sm);
   DecodeArgs A;
   A.q = static_cast<const __nv_bfloat16*>(q);
@@ -766,7 +771,7 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.lse = lse;
   A.logits = logits;
   A.status = status;
-  cudaError_t e = launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
   if (e != cudaSuccess) return SA_ERR_CUDA;
   e = launch_pdl(merge_chunks_kernel, dim3(p.G, U), dim3(kMergeThreads), 0, stream, p,
                  static_cast<const float*>(partials), static_cast<const int*>(counters), out, lse);
