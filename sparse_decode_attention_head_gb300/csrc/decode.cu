@@ -738,8 +738,9 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
                        int* ticket, cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
-  if (smem > 48 * 1024)
-    smem_limit_at_least(reinterpret_cast<const void*>(build_tiles_kernel), (int)smem);
+  // static + dynamic shared memory can pass the 48 KB default even when the
+  // dynamic part alone does not: always opt in (cached per kernel)
+  smem_limit_at_least(reinterpret_cast<const void*>(build_tiles_kernel), (int)smem);
   dim3 grid(p.Hk, p.B);
   const cudaError_t e = launch_pdl(build_tiles_kernel, grid, dim3(kBuildThreads), smem, stream, p, seq_lens,
                                    page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, out, lse,

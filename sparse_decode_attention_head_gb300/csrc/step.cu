@@ -62,8 +62,9 @@ int launch_build_step(const Params& p, const int* seq_lens, const int* page_tabl
                       void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
                       cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
-  if (smem > 48 * 1024)
-    smem_limit_at_least(reinterpret_cast<const void*>(build_step_kernel), (int)smem);
+  // static + dynamic shared memory can pass the 48 KB default even when the
+  // dynamic part alone does not: always opt in (cached per kernel)
+  smem_limit_at_least(reinterpret_cast<const void*>(build_step_kernel), (int)smem);
   const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
                                    seq_lens, page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
@@ -188,7 +189,7 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
   }
 #undef SA_SB_PICK
   if (kern == nullptr) return SA_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024) smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
+  smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
   const cudaError_t e = launch_pdl(kern, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p, scores, seq_lens,
                                    page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),

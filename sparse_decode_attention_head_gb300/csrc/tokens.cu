@@ -131,7 +131,7 @@ int launch_token_topk(const Params& p, const void* q, const void* k_pool, const 
   } else {
     return SA_ERR_UNSUPPORTED;
   }
-  if (smem > 48 * 1024) smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
+  smem_limit_at_least(reinterpret_cast<const void*>(kern), (int)smem);
   const cudaError_t e = launch_pdl(kern, grid, dim3(nt), smem, stream, p, qb, kb, page_table, seq_lens, cand_idx,
                                    cand_cnt, sel_idx, sel_cnt, scores_out, status);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;

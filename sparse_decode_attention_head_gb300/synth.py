@@ -110,6 +110,17 @@ def workload(name: str) -> Workload:
     raise KeyError(name)
 
 
+def sweep_workload(B: int, ctx: int, budget_bp: int, extra_tokens: int = 16) -> Workload:
+    """One cell of the throughput sweep of the full decode-attention stack:
+    a Llama-3-8B-shaped layer (32 q / 8 KV heads, page = block = 16, 4 sinks,
+    window 1024), batch B, context ctx, budget budget_bp basis points of the
+    candidate blocks (10000 = dense), room for extra_tokens appended tokens;
+    planted sink, 1 % heavy blocks and the 2K recency ramp of the 32K layer."""
+    return Workload(f"sweep_b{B}_ctx{ctx}_bp{budget_bp}", B=B, Hq=32, Hk=8, L=ctx, block_sizes=[16] * 8,
+                    budget_bp=[budget_bp] * 8, S=4, W=1024, c_heavy=1.5, heavy_frac=0.01, recency=2048,
+                    extra_tokens=extra_tokens)
+
+
 # --------------------------------------------------------------------------
 # partition helpers (pure integer bookkeeping, shared by the harness)
 # --------------------------------------------------------------------------
