@@ -650,6 +650,100 @@ def run_bypass(args, dev, rank, reps=200):
             "speedup": round(res["plain"]["ms_per_step"] / res["bypass"]["ms_per_step"], 3)}
 
 
+SWEEP_BATCH = (1, 4, 16, 64)
+SWEEP_CTX = (8192, 32768, 131072, 262144)
+SWEEP_BUDGET_BP = (100, 500, 1000, 10000)
+SWEEP_LAYERS = 32
+SWEEP_STEPS = 16
+SWEEP_KV_CAP = 150e9
+
+
+def run_sweep(args):
+    """The throughput sweep of the full decode-attention stack: 32
+    Llama-3-8B-shaped layers (distinct KV caches), batch x context x budget,
+    16 decode steps each appending one token per sequence per layer
+    (sa_decode_step_append), cells whose KV exceeds 150 GB left out.  The
+    16 x 32 layer-steps of a cell are one CUDA graph, replayed between CUDA
+    events.  One JSON line per cell."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sa.lib()
+    st = torch.cuda.Stream(device=dev)
+    for B in SWEEP_BATCH:
+        for ctx in SWEEP_CTX:
+            kv = SWEEP_LAYERS * B * ctx * 8 * 16 * 128 * 2 * 2 / 16
+            if kv > SWEEP_KV_CAP:
+                print(json.dumps({"sweep_cell": {"batch": B, "context": ctx}, "skipped": f"KV {kv / 1e9:.0f} GB > 150 GB"}),
+                      flush=True)
+                continue
+            base = synth.sweep_workload(B, ctx, SWEEP_BUDGET_BP[0], extra_tokens=SWEEP_STEPS)
+            layers = []
+            for l in range(SWEEP_LAYERS):
+                c = synth.make_decode_case(base, 7000 + l, device=dev)
+                layers.append(dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens))
+                del c
+            g = torch.Generator(device=dev).manual_seed(99)
+            k_new = torch.randn(SWEEP_STEPS, B, 8, 128, generator=g, device=dev).to(torch.bfloat16)
+            v_new = torch.randn(SWEEP_STEPS, B, 8, 128, generator=g, device=dev).to(torch.bfloat16)
+            lens = [torch.full((B,), ctx + s + 1, dtype=torch.int32, device=dev) for s in range(SWEEP_STEPS)]
+            summ = None
+            for bp in SWEEP_BUDGET_BP:
+                wl = synth.sweep_workload(B, ctx, bp, extra_tokens=SWEEP_STEPS)
+                ks = synth.k_per_qhead(wl, ctx + SWEEP_STEPS)
+                prob = sa.Problem(B=B, Hq=32, Hk=8, max_pages_per_seq=wl.max_pages_per_seq,
+                                  num_pages=B * wl.max_pages_per_seq, sink=wl.S, window=wl.W,
+                                  block_sizes=wl.block_sizes, k_per_head=ks, kcap=max(1, max(ks)),
+                                  mode=sa.SUMMARY_MINMAX)
+                ws = sa.Workspace(prob, device=dev)
+                if summ is None:   # the prefill's summaries, one build per layer (budget-independent)
+                    summ = []
+                    for L in layers:
+                        t = torch.empty(prob.summary_shape(), dtype=torch.bfloat16, device=dev)
+                        sa.block_summarize(prob, L["k"], L["pt"], L["sl"], t, ws)
+                        summ.append(t)
+                idx = torch.empty(B, 32, prob.kcap, dtype=torch.int32, device=dev)
+                cnt = torch.empty(B, 32, dtype=torch.int32, device=dev)
+                out = torch.empty(B, 32, 128, device=dev)
+                lse = torch.empty(B, 32, device=dev)
+
+                def stack():
+                    for s in range(SWEEP_STEPS):
+                        for l, L in enumerate(layers):
+                            sa.decode_step_append(prob, L["q"], k_new[s], v_new[s], L["k"], L["v"], L["pt"], lens[s],
+                                                  summ[l], idx, cnt, out, lse, ws)
+
+                with torch.cuda.stream(st):
+                    stack()   # eager pass: kernel attributes, and the appended rows in place
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(st):
+                    with torch.cuda.graph(gr, stream=st, capture_error_mode="relaxed"):
+                        stack()
+                gr.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(st):
+                    e0.record(st)
+                    gr.replay()
+                    e1.record(st)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1)
+                status = ws.status()
+                # algorithmic bytes of the last layer-step (its selection), times the layer-steps
+                nb = algorithmic_bytes(wl, prob, lens[-1].cpu().numpy(), idx, cnt)["total"]
+                step_ms = ms / SWEEP_STEPS
+                print(json.dumps({
+                    "sweep_cell": {"batch": B, "context": ctx, "budget": bp / 10000, "layers": SWEEP_LAYERS,
+                                   "steps": SWEEP_STEPS, "kv_gb": round(kv / 1e9, 1)},
+                    "ms_per_token_step": round(step_ms, 4), "tokens_per_s": round(B / (step_ms / 1e3), 1),
+                    "layer_queries_per_s": round(B * 32 * SWEEP_LAYERS / (step_ms / 1e3), 1),
+                    "algorithmic_gb_per_s": round(nb * SWEEP_LAYERS / (step_ms / 1e3) / 1e9, 1),
+                    "status": status}), flush=True)
+                del gr, ws, idx, cnt
+            del layers, summ, k_new, v_new
+            torch.cuda.empty_cache()
+
+
 # --------------------------------------------------------------------------- oracle timing
 
 def cpu_baseline(L, wl, ks, scale, budget_s=15.0, units=None):
@@ -722,11 +816,15 @@ def main():
     ap.add_argument("--no-tables", action="store_true", help="skip the score-table (a7) leg")
     ap.add_argument("--no-group", action="store_true", help="skip the group-shared selection variant")
     ap.add_argument("--no-bypass", action="store_true", help="skip the head-sparsity bypass variant")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the batch x context x budget throughput sweep of a 32-layer stack (one line per cell)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 
