@@ -22,25 +22,8 @@
 
 #include <mutex>
 
-#include "sa_common.cuh"
+#include "launch.cuh"
 
-namespace sa {
-int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
-                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       int* ticket, cudaStream_t stream);
-int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
-                  float* partials, int* counters, float* out, float* lse, float* logits, int* status,
-                  const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
-size_t decode_smem_bytes(int U);
-size_t decode_partials_bytes(const Params& p);
-size_t tiles_bytes(const Params& p);
-}  // namespace sa
-
-namespace sa_host {
-int make_params(const sa_problem* pr, sa::Params* p);
-int make_kv_map(CUtensorMap* m, const void* pool, const sa::Params& p);
-int num_sms_current();
-}  // namespace sa_host
 
 namespace {
 
