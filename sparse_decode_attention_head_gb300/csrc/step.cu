@@ -122,7 +122,7 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
   const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int G = p.G;
   const int win = min(p.mpp, kWinPages);
-  int* s_sel = smem_b + 5 * win;
+  int* s_sel = smem_b + build_smem_bytes(p.mpp) / sizeof(int);
   int* s_cnt = s_sel + G * p.kcap;
   const int L = min(seq_lens[b], p.mpp * kP);
   const uint32_t active = unit_active_heads(p, b, kvh);   // loaded now, used after the top-k

@@ -38,12 +38,13 @@ __device__ __forceinline__ uint32_t unit_active_heads(const Params& p, int b, in
 }
 
 // Pages per builder window: the builder keeps a flag and 16 token masks per
-// page of the current window in shared memory (20 bytes a page).
+// page of the current window in shared memory (20 bytes a page, plus 16 so
+// that the masks can start on a 16-byte boundary).
 constexpr int kWinPages = 4096;
 
 __host__ __device__ inline size_t build_smem_bytes(int mpp) {
   const int w = mpp < kWinPages ? mpp : kWinPages;
-  return (size_t)w * (sizeof(int) + 4 * sizeof(uint32_t));
+  return (size_t)w * (sizeof(int) + 4 * sizeof(uint32_t)) + 16;
 }
 
 // Collective over threads [0, NT) (named barrier 1): build the tile list of
@@ -53,7 +54,8 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
 // then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
 // a block scan of the page flags, and one 32-byte store per tile.
 // sel_row: the unit's selections [G][kcap] (global or shared memory),
-// cnt_row: their counts [G].  active: the heads that attend (G bits); the
+// cnt_row: their counts [G].  A page's four mask words are one 16-byte
+// access (conflict-free across a warp's contiguous page ranges).  active: the heads that attend (G bits); the
 // others are left out -- no tokens attend for them and their output rows are
 // not written.  s_flag: window ints, s_mask: 4 window words,
 // scan_tmp: 32 ints.
@@ -67,6 +69,7 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   constexpr int kPer = (kWinPages + NT - 1) / NT;   // pages per thread and window, at most
   constexpr int kItemRegs = 2;                      // selection entries prefetched per thread (r = 0, 1 below)
   auto bsync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); };
+  s_mask = reinterpret_cast<uint32_t*>((reinterpret_cast<uintptr_t>(s_mask) + 15) & ~uintptr_t(15));
   const int u = b * p.Hk + kvh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
@@ -108,19 +111,18 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
     const int a = min(wn, tid * per), e = min(wn, a + per);
     // dense-set tokens of each page attend for every head
     for (int i = a; i < e; ++i) {
-      uint32_t any = 0;
+      uint32_t m[4];
 #pragma unroll
       for (int w4 = 0; w4 < 4; ++w4) {
-        uint32_t m = 0;
+        m[w4] = 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int tok = (w0 + i) * kP + 4 * w4 + r;
-          if (tok < Lc && (tok < s_end || tok >= w_beg)) m |= all << (8 * r);
+          if (tok < Lc && (tok < s_end || tok >= w_beg)) m[w4] |= all << (8 * r);
         }
-        s_mask[4 * i + w4] = m;
-        any |= m;
       }
-      s_flag[i] = any != 0;
+      reinterpret_cast<uint4*>(s_mask)[i] = make_uint4(m[0], m[1], m[2], m[3]);
+      s_flag[i] = (m[0] | m[1] | m[2] | m[3]) != 0;
     }
     bsync();
     // each head's selected tokens inside M (and inside this window)
@@ -183,7 +185,8 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
         if (!ok) set_status(status, SA_ERR_BAD_PAGE);
         int4* dst = reinterpret_cast<int4*>(T + idx);
         dst[0] = make_int4(w0 + i, ok ? ph : -1, 0, 0);
-        dst[1] = make_int4((int)s_mask[4 * i], (int)s_mask[4 * i + 1], (int)s_mask[4 * i + 2], (int)s_mask[4 * i + 3]);
+        const uint4 mv = reinterpret_cast<const uint4*>(s_mask)[i];
+        dst[1] = make_int4((int)mv.x, (int)mv.y, (int)mv.z, (int)mv.w);
         ++idx;
       }
     }
