@@ -329,3 +329,24 @@ def test_prepared_step_call_matches_decode_step():
         assert torch.equal(c1, cnt) and torch.equal(i1, idx)
         H.assert_close(o1.cpu().numpy(), out.cpu().numpy(), "prepared O")
         H.assert_close(l1.cpu().numpy(), lse.cpu().numpy(), "prepared lse")
+
+
+@pytest.mark.parametrize("G", [1, 2, 5, 6, 8])
+def test_group_sizes(G):
+    # every group size the kernels are instantiated for beyond 3, 4 and 7 (8 is the largest)
+    wl = _small(name=f"g{G}", B=2, Hq=2 * G, Hk=2, block_sizes=[16, 32], budget_bp=[1000, 700],
+                lens=[1500, 1111])
+    prob, dev, ws, nc, ref_sel = _full_pipeline(wl, 5 + G, "minmax")
+    # the fused step (scores, top-k + tiles + tail summary, decode, merge) on fresh summaries
+    summ = H.gpu_summaries(prob, dev, ws)
+    idx = torch.full((wl.B, wl.Hq, prob.kcap), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((wl.B, wl.Hq), -5, dtype=torch.int32, device="cuda")
+    out = torch.full((wl.B, wl.Hq, wl.D), float("nan"), device="cuda")
+    lse = torch.full((wl.B, wl.Hq), float("nan"), device="cuda")
+    sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx, cnt,
+                   out, lse, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    _check_selection(prob, wl, nc, idx, cnt, None, ref_sel)
+    ref_dec = H.oracle_decode(nc, wl, {k: v[0] for k, v in ref_sel.items()}, sa.SEL_BLOCK, prob.scale)
+    _check_decode(out, lse, ref_dec)
