@@ -350,9 +350,7 @@ size_t topk_smem_bytes(const Params&) { return 0; }
 int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* sel_idx, int* sel_cnt,
                 cudaStream_t stream) {
   dim3 grid(p.sel_mode == SA_SELECT_GROUP ? p.Hk : p.Hq, p.B);
-  // the largest candidate count any head can have
-  int max_n = 0;
-  for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  const int max_n = max_candidates(p);
   const bool grp = p.sel_mode == SA_SELECT_GROUP;
   cudaError_t e;
   if (max_n <= 256 * 8)

@@ -170,8 +170,7 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
                         void* k_pool, void* v_pool, const void* k_new, const void* v_new, float* stats, void* summ,
                         int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status,
                         int* ticket, cudaStream_t stream) {
-  int max_n = 0;
-  for (int h = 0; h < p.Hk; ++h) max_n = std::max(max_n, (p.mpp * kP + p.bs[h] - 1) / p.bs[h]);
+  const int max_n = max_candidates(p);
   const size_t smem = build_smem_bytes(p.mpp) + ((size_t)p.G * p.kcap + p.G) * sizeof(int);
   if (smem > 160 * 1024) return SA_ERR_UNSUPPORTED;
   void (*kern)(Params, const float*, const int*, const int*, __nv_bfloat16*, __nv_bfloat16*, const __nv_bfloat16*,

@@ -8,6 +8,8 @@
 // index order.
 #pragma once
 
+#include <algorithm>
+
 #include "sa_common.cuh"
 
 namespace sa {
@@ -21,6 +23,17 @@ __device__ __forceinline__ void group_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+
+// The most candidate blocks any head can have: candidates end where the
+// recent window begins, at ceil(max(L - W, S) / Bs) <= ceil(max(mpp P - W, S) / Bs).
+inline int max_candidates(const Params& p) {
+  int m = 0;
+  for (int h = 0; h < p.Hk; ++h) {
+    const int w_beg = std::max(p.mpp * kP - p.W, std::min(p.S, p.mpp * kP));
+    m = std::max(m, (w_beg + p.bs[h] - 1) / p.bs[h]);
+  }
+  return m;
+}
 
 struct TopkScratch {
   int hist[256];
