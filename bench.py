@@ -669,14 +669,20 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     sa.lib()
     st = torch.cuda.Stream(device=dev)
+    only = None   # --sweep-cells B:ctx:bp,... restricts the sweep to those cells
+    if args.sweep_cells:
+        only = {tuple(int(v) for v in c.split(":")) for c in args.sweep_cells.split(",")}
     for B in SWEEP_BATCH:
         for ctx in SWEEP_CTX:
+            budgets = [bp for bp in SWEEP_BUDGET_BP if only is None or (B, ctx, bp) in only]
+            if not budgets:
+                continue
             kv = SWEEP_LAYERS * B * ctx * 8 * 16 * 128 * 2 * 2 / 16
             if kv > SWEEP_KV_CAP:
                 print(json.dumps({"sweep_cell": {"batch": B, "context": ctx}, "skipped": f"KV {kv / 1e9:.0f} GB > 150 GB"}),
                       flush=True)
                 continue
-            base = synth.sweep_workload(B, ctx, SWEEP_BUDGET_BP[0], extra_tokens=SWEEP_STEPS)
+            base = synth.sweep_workload(B, ctx, budgets[0], extra_tokens=SWEEP_STEPS)
             layers = []
             for l in range(SWEEP_LAYERS):
                 c = synth.make_decode_case(base, 7000 + l, device=dev)
@@ -687,7 +693,7 @@ def run_sweep(args):
             v_new = torch.randn(SWEEP_STEPS, B, 8, 128, generator=g, device=dev).to(torch.bfloat16)
             lens = [torch.full((B,), ctx + s + 1, dtype=torch.int32, device=dev) for s in range(SWEEP_STEPS)]
             summ = None
-            for bp in SWEEP_BUDGET_BP:
+            for bp in budgets:
                 wl = synth.sweep_workload(B, ctx, bp, extra_tokens=SWEEP_STEPS)
                 ks = synth.k_per_qhead(wl, ctx + SWEEP_STEPS)
                 prob = sa.Problem(B=B, Hq=32, Hk=8, max_pages_per_seq=wl.max_pages_per_seq,
@@ -818,6 +824,8 @@ def main():
     ap.add_argument("--no-bypass", action="store_true", help="skip the head-sparsity bypass variant")
     ap.add_argument("--sweep", action="store_true",
                     help="the batch x context x budget throughput sweep of a 32-layer stack (one line per cell)")
+    ap.add_argument("--sweep-cells", default="",
+                    help="with --sweep: only these cells, as batch:context:budget_bp[,...]")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
