@@ -51,15 +51,15 @@ Readings where the pages are silent (each also listed in the design notes):
       slash by offset (L - 1 - i); one threshold tau = beta / |I|, strict
       comparison; expansion {-1, 0, 1, 2} clipped to M; at most kcap tokens
       (lowest positions kept).
+  R9  Group-shared selection (a variant; the pages select per head): the
+      blocks of a KV head are ranked by the fp32 sum, in head order, of its G
+      query heads' canonical scores; every head of the group keeps the same k
+      blocks (ties by lower block index).
   R10 Exact top-k inside the table candidates (LFPS, "The reading": an exact
       top-k needs a dot product against every key; the tables only narrow the
       keys down): each candidate token's score is the canonical fp32 dot
       product of q with its bf16 key row (reading R4's order), and the k best
       by (score descending, position ascending) are kept, reported ascending.
-  R9  Group-shared selection (a variant; the pages select per head): the
-      blocks of a KV head are ranked by the fp32 sum, in head order, of its G
-      query heads' canonical scores; every head of the group keeps the same k
-      blocks (ties by lower block index).
   R11 Head-sparsity bypass (LFPS Algorithm 1 step 1, Eq. (5), Eq. (6),
       App. B.1; epsilon = 0.85): tokens split into the sink (token 0), the
       local window (the six newest of the L keys) and the n global tokens
