@@ -124,3 +124,29 @@ def test_bypass_entries_validate_before_launch(lib):
         == sa.SA_ERR_INVALID_ARG                                            # k_new without v_new
     bad = _prob(D=64)
     assert lib.sa_kv_stats(bad.ref, vp, vp, vp, vp, vp, vp, None) == sa.SA_ERR_INVALID_ARG
+
+
+def test_every_compute_call_refuses_host_tensors():
+    # no CPU fallback: each call of the binding wants device tensors and says so
+    import torch
+    p = _prob()
+    t = torch.zeros(4)
+    ws = object()   # never reached
+    calls = [
+        lambda: sa.block_summarize(p, t, t, t, t, ws),
+        lambda: sa.select_topk(p, t, t, t, t, t, ws),
+        lambda: sa.sparse_decode(p, t, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.decode_step(p, t, t, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.decode_step_append(p, t, t, t, t, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.append_kv(p, t, t, t, t, t, t, ws),
+        lambda: sa.select_tokens(p, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.update_score_tables(p, t, t, t, t, t, t, t, ws),
+        lambda: sa.kv_stats(p, t, t, t, t, t, ws),
+        lambda: sa.head_sparsity(p, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.decode_step_bypass(p, t, t, t, t, t, t, t, t, t, t, t, t, ws),
+        lambda: sa.lse_merge(torch.zeros(2, 128), torch.zeros(2), torch.zeros(2, 128), torch.zeros(2),
+                             torch.zeros(2, 128), torch.zeros(2)),
+    ]
+    for c in calls:
+        with pytest.raises(TypeError, match="CUDA tensor"):
+            c()
