@@ -49,8 +49,11 @@
  *     workspace; the offending work is skipped, nothing traps.  Read it with
  *     sa_get_status().
  *   - Scratch comes from a caller-allocated workspace of sa_workspace_size()
- *     bytes, zeroed once with sa_workspace_init().  Calls that share one
- *     workspace must be ordered on one stream.
+ *     bytes (16-byte aligned), zeroed once with sa_workspace_init().  Calls
+ *     that share one workspace must be ordered on one stream.
+ *   - Alignment: q, the K / V pools, summaries, out and the workspace must be
+ *     16-byte aligned (the kernels move them 16 bytes at a time); a
+ *     misaligned pointer returns SA_ERR_INVALID_ARG before any launch.
  */
 #ifndef SA_H_
 #define SA_H_
@@ -150,8 +153,14 @@ int sa_block_summarize(const sa_problem* prob, const void* k_pool,
                        int32_t block_begin, int32_t block_end, void* summaries,
                        void* ws, void* stream);
 
-/* Step a2 -- block scores.  For every (b, query head h) and candidate block j:
- * MINMAX  s = sum_d q_d * (q_d >= 0 ? kmax_d : kmin_d)
+/* Step a2 -- block scores.  Fluxion (core claim; Fig. 2d, where the top-k
+ * cost grows as blocks shrink) ranks KV blocks per head, and LFPS ("The
+ * reading") notes that an exact top-k needs a dot product against every
+ * key; the pages do not define the block score itself.  The score taken
+ * here is the dot product of q with the block summary of sa_block_summarize:
+ * for every (b, query head h) and candidate block j,
+ * MINMAX  s = sum_d q_d * (q_d >= 0 ? kmax_d : kmin_d)  (the largest q.k any
+ *         key inside the block's min/max box can reach)
  * MEAN    s = sum_d q_d * kmean_d
  * in fp32 in the canonical order: the 128 dims form 8 lanes of 16
  * consecutive dims, each lane sums its exact products in ascending dim order
@@ -180,7 +189,11 @@ int sa_select_topk(const sa_problem* prob, const void* q,
                    void* ws, void* stream);
 
 /* Steps a4 + a5 + a6 -- paged gather split-K decode attention with the exact
- * log-sum-exp merge.  For every (b, h): attend q[b][h] over I plus the
+ * log-sum-exp merge.  HGCA (review, "What carries the argument") attends the
+ * newest entries densely and selected older entries sparsely and fuses the
+ * two partial outputs with the identity above; SPIN (abstract, Fig. 6) keeps
+ * the KV in pages reached through a page table; Fluxion (Fig. 4) keeps the
+ * attention sinks.  For every (b, h): attend q[b][h] over I plus the
  * head's selected set J_h = (entries of sel_idx[b][h][0..sel_cnt)) inside M,
  * with z_t = scale * q.k_t:
  *   out[b][h][:] = sum_t softmax(z)_t v_t  (fp32), lse[b][h] = log sum e^{z_t}.
@@ -286,7 +299,8 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in,
  * cannot hand sa_sparse_decode a workspace -- for example code running inside
  * a host framework that owns every device allocation through its own pool,
  * or a latency-critical path where cudaMalloc's implicit synchronisation is
- * not allowed.  Same inputs, outputs and results as sa_sparse_decode; the
+ * not allowed.  The inputs, outputs and results of sa_sparse_decode with
+ * bypass_or_null = NULL: there is no bypass input, every head attends.  The
  * scratch lives in a fixed 64 MiB array of device memory inside the library
  * (held by every GPU that loads the library until the process exits).
  * The call allocates nothing.  A problem whose scratch does not fit returns
@@ -295,8 +309,9 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in,
  *   error of this call (SA_OK otherwise); it is zeroed at the start of the
  *   call.  When NULL, device-side errors are recorded only inside the library.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the array and it keeps the last
+ * (cudaGetSymbolAddress) with that device current, and again after the
+ * device's context changes (cudaDeviceReset); make that first call before
+ * any stream capture.  All calls share the array and it keeps the last
  * call's contents (the counters and status it needs zeroed are cleared at the
  * start of each call): calls that overlap on the GPU race with each other. */
 int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q,

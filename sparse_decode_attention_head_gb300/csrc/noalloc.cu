@@ -14,7 +14,8 @@
 //
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
-// that device current) and caches it.  Every call shares the array and it
+// that device current) and caches it with the id of the context it belongs
+// to (a reset device, or another context on it, is looked up again).  Every call shares the array and it
 // keeps the last call's contents: the status word is cleared at the start of
 // each call (the tile builder zeroes the chunk ticket), and two calls that overlap on the
 // GPU (different streams, or different host threads) race on it.
@@ -33,7 +34,43 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+// The array's device address belongs to a CUDA context, not to a device
+// ordinal: after cudaDeviceReset, or under another driver-API context, the
+// same ordinal has a different context and the array a different address.
+// The address is therefore cached with the unique id of the context it was
+// looked up in (cuCtxGetId; ids are never reused within a process).
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current context, or 0 if it cannot be had (then the
+// address is looked up again on every call).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -58,18 +95,23 @@ NoAllocLayout layout_of(const sa::Params& p) {
   return l;
 }
 
-// Device address of the scratch array on the current device (set-up on first use).
+// Device address of the scratch array in the current context (looked up on
+// the first call in that context, with its device current).
 int scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+  unsigned long long id = current_context_id();   // 0 before the runtime has made a context current
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchEntry& e = g_scratch[dev];
+  if (e.ptr == nullptr || id == 0 || e.ctx_id != id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return SA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    if (id == 0) id = current_context_id();   // the lookup itself has made the context current
+    e.ptr = ptr;
+    e.ctx_id = id;
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return SA_OK;
 }
 
@@ -88,7 +130,7 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !sel_idx || !sel_cnt || !out || !lse)
     return SA_ERR_INVALID_ARG;
   if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const NoAllocLayout l = layout_of(p);

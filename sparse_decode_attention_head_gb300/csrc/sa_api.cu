@@ -228,7 +228,7 @@ int sa_block_summarize(const sa_problem* prob, const void* k_pool, const int32_t
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
   if (!k_pool || !page_table || !seq_lens || !summaries || !ws) return SA_ERR_INVALID_ARG;
-  if (!aligned16(k_pool) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(summaries) || !aligned16(ws)) return SA_ERR_INVALID_ARG;
   if (block_begin < 0 && block_begin != SA_BLOCKS_TAIL) return SA_ERR_INVALID_ARG;
   if (block_end < -1) return SA_ERR_INVALID_ARG;
   const Layout l = layout_of(p);
@@ -242,7 +242,7 @@ int sa_score_blocks(const sa_problem* prob, const void* q, const void* summaries
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
   if (!q || !summaries || !seq_lens || !scores || !ws) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summaries) || !aligned16(ws)) return SA_ERR_INVALID_ARG;
   const int nsm = num_sms_current();
   if (nsm <= 0) return SA_ERR_CUDA;
   return sa::launch_score(p, q, summaries, seq_lens, scores, 1, nsm, as_stream(stream), nullptr);
@@ -254,7 +254,7 @@ int sa_select_topk(const sa_problem* prob, const void* q, const void* summaries,
   int rc = make_params(prob, &p);
   if (rc != SA_OK) return rc;
   if (!q || !summaries || !seq_lens || !sel_idx || !sel_cnt || !ws) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summaries) || !aligned16(ws)) return SA_ERR_INVALID_ARG;
   if (sa::topk_smem_bytes(p) > 200 * 1024) return SA_ERR_UNSUPPORTED;
   const Layout l = layout_of(p);
   float* scores = scores_or_null ? scores_or_null : at<float>(ws, l.scores);
@@ -277,7 +277,10 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !sel_idx || !sel_cnt || !out || !lse || !ws)
     return SA_ERR_INVALID_ARG;
   if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return SA_ERR_INVALID_ARG;
+  // the kernels read q, K, V with 16-byte copies and store out and the
+  // workspace's tiles and partials 16 bytes at a time
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(ws))
+    return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
   if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const int nsm = num_sms_current();
@@ -314,7 +317,9 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !summaries || !sel_idx || !sel_cnt || !out || !lse ||
       !ws)
     return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summaries)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summaries) || !aligned16(out) ||
+      !aligned16(ws))
+    return SA_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return SA_ERR_INVALID_ARG;
   if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;

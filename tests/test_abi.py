@@ -150,3 +150,23 @@ def test_every_compute_call_refuses_host_tensors():
     for c in calls:
         with pytest.raises(TypeError, match="CUDA tensor"):
             c()
+
+
+def test_misaligned_out_or_workspace_rejected_before_launch(lib):
+    # the kernels store out and the workspace's tiles and partials 16 bytes at
+    # a time: a pointer that is only 4-byte aligned is refused on the host
+    # (these calls return before any launch; the pointers are never dereferenced)
+    p = _prob()
+    a, m = ctypes.c_void_p(256), ctypes.c_void_p(260)
+    bad = sa.SA_ERR_INVALID_ARG
+    assert lib.sa_sparse_decode(p.ref, a, a, a, a, a, a, a, 0, m, a, None, None, a, None) == bad   # out
+    assert lib.sa_sparse_decode(p.ref, a, a, a, a, a, a, a, 0, a, a, None, None, m, None) == bad   # ws
+    assert lib.sa_decode_step(p.ref, a, a, a, a, a, a, a, a, m, a, a, None) == bad                  # out
+    assert lib.sa_decode_step(p.ref, a, a, a, a, a, a, a, a, a, a, m, None) == bad                  # ws
+    assert lib.sa_decode_step_append(p.ref, a, a, a, a, a, a, a, a, a, a, m, a, a, None) == bad     # out
+    assert lib.sa_decode_step_bypass(p.ref, a, None, None, a, a, a, a, a, a, 0.85, a, a, m, a, None, a, a,
+                                     None) == bad                                                   # out
+    assert lib.sa_sparse_decode_noalloc(p.ref, a, a, a, a, a, a, a, 0, m, a, None, None, None) == bad
+    assert lib.sa_block_summarize(p.ref, a, a, a, 0, -1, a, m, None) == bad                         # ws
+    assert lib.sa_score_blocks(p.ref, a, a, a, a, m, None) == bad                                   # ws
+    assert lib.sa_select_topk(p.ref, a, a, a, a, a, None, m, None) == bad                           # ws

@@ -1,0 +1,136 @@
+"""The whole decode step (sa_decode_step: tail-summary refresh, block scores,
+per-head top-k, paged sparse decode, exact LSE merge) against the fp64 oracle.
+
+This is the call the throughput benchmark times, so it is compared with the
+oracle directly: selected block index sets bit for bit (Fluxion core claim:
+per-head block top-k), O and lse within max-abs 2e-3 / max-rel 1e-2 (HGCA
+review, "What carries the argument": the merged output), the refreshed tail
+summaries bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sparse_attention_oracle as orc
+from sparse_decode_attention_head_gb300 import sa, synth
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    sa.lib()
+
+
+def _small(name="small", **kw):
+    base = dict(B=3, Hq=6, Hk=2, L=1500, block_sizes=[8, 64], budget_bp=[1500, 800], S=4, W=96,
+                c_heavy=2.0, heavy_count=4, recency=300)
+    base.update(kw)
+    return synth.Workload(name, **base)
+
+
+def _run_step(prob, dev, summ, ws):
+    idx = torch.full((prob.B, prob.Hq, prob.kcap), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((prob.B, prob.Hq), -5, dtype=torch.int32, device="cuda")
+    out = torch.full((prob.B, prob.Hq, prob.D), float("nan"), device="cuda")
+    lse = torch.full((prob.B, prob.Hq), float("nan"), device="cuda")
+    sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx, cnt,
+                   out, lse, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    return idx, cnt, out, lse
+
+
+def _poison_tails(summ, nc, wl):
+    for b in range(wl.B):
+        L = int(nc.seq_lens[b])
+        for kvh in range(wl.Hk):
+            if L > 0:
+                summ[b, kvh, (L - 1) // wl.block_sizes[kvh]] = 3.0
+
+
+def _step_vs_oracle(wl, seed, mode, units=None, ks=None, repeat=1):
+    case = synth.make_decode_case(wl, seed)
+    nc = H.to_np_case(case)
+    ks = synth.k_per_qhead(wl) if ks is None else ks
+    prob = H.make_problem(wl, ks, mode=mode)
+    dev = H.to_dev(case)
+    ws = sa.Workspace(prob)
+    summ = H.gpu_summaries(prob, dev, ws)
+    _poison_tails(summ, nc, wl)
+    units = units or [(b, k) for b in range(wl.B) for k in range(wl.Hk)]
+    ref_sel = H.oracle_select(nc, wl, ks, mode, units)
+    ref_dec = H.oracle_decode(nc, wl, {k: v[0] for k, v in ref_sel.items()}, sa.SEL_BLOCK, prob.scale, units)
+    for _ in range(repeat):   # back-to-back steps on one workspace give the same results
+        idx, cnt, out, lse = _run_step(prob, dev, summ, ws)
+        si, sc, o, l = idx.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
+        for (b, h), (sel, _, _) in ref_sel.items():
+            n = int(sc[b, h])
+            assert n == len(sel), f"(b={b}, h={h}) count {n} vs {len(sel)}"
+            assert np.array_equal(si[b, h, :n], sel), f"(b={b}, h={h}) index set differs"
+            O, lz = ref_dec[(b, h)]
+            H.assert_close(o[b, h], O, f"O(b={b},h={h})")
+            H.assert_close(np.array([l[b, h]]), np.array([lz]), f"lse(b={b},h={h})")
+    # the tail block of every unit was refreshed from the keys
+    sg = summ.float().cpu().numpy()
+    for b, kvh in units:
+        L = int(nc.seq_lens[b])
+        if L == 0:
+            continue
+        last = (L - 1) // wl.block_sizes[kvh]
+        ref = H.oracle_summaries(nc, wl, b, kvh, mode, last, last + 1)
+        assert np.array_equal(sg[b, kvh, last], ref[0]), f"tail summary differs at b={b} kvh={kvh}"
+    return prob, dev, ws, nc
+
+
+@pytest.mark.parametrize("mode", ["minmax", "mean"])
+def test_step_llama_32k_full_size_vs_oracle(mode):
+    # every (sequence, head) of the 32K Llama-shaped layer the benchmark times
+    _step_vs_oracle(synth.workload("llama_32k"), 31, mode)
+
+
+@pytest.mark.parametrize("mode", ["minmax", "mean"])
+def test_step_qwen_64k_sampled_vs_oracle(mode):
+    # G = 7, block size and budget drawn per KV head; one sampled unit per KV head
+    wl = synth.workload("qwen_64k")
+    _step_vs_oracle(wl, 32, mode, units=[(0, 0), (6, 1), (9, 2), (15, 3)])
+
+
+@pytest.mark.parametrize("mode", ["minmax", "mean"])
+def test_step_ragged_mixed_block_sizes_vs_oracle(mode):
+    _step_vs_oracle(_small(lens=[1500, 1013, 333]), 33, mode, repeat=3)
+
+
+def test_step_short_and_empty_sequences_vs_oracle():
+    # L = 0 (O = 0, lse = -inf), L < S, L < S + W (dense only), L = 1
+    _step_vs_oracle(_small(B=4, lens=[0, 3, 77, 1], L=100, heavy_count=0, recency=0), 34, "minmax", repeat=2)
+
+
+def test_step_full_and_zero_budget_vs_oracle():
+    wl = _small(B=2, lens=[1500, 999])
+    ks = []
+    for h in range(wl.Hq):
+        j0, j1 = orc.candidate_blocks(1500, wl.S, wl.W, wl.block_sizes[h // wl.G])
+        ks.append(j1 - j0 if h % 2 == 0 else 0)
+    _step_vs_oracle(wl, 35, "minmax", ks=ks)
+
+
+def test_step_tiny_4k_new_inputs_each_call():
+    # one workspace, fresh q and keys on every call: nothing of a previous step leaks into the next
+    wl = synth.workload("tiny_4k")
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    ws = sa.Workspace(prob)
+    for seed in (36, 37, 38):
+        case = synth.make_decode_case(wl, seed)
+        nc = H.to_np_case(case)
+        dev = H.to_dev(case)
+        summ = H.gpu_summaries(prob, dev, ws)
+        idx, cnt, out, lse = _run_step(prob, dev, summ, ws)
+        ref_sel = H.oracle_select(nc, wl, ks, "minmax")
+        ref = H.oracle_decode(nc, wl, {k: v[0] for k, v in ref_sel.items()}, sa.SEL_BLOCK, prob.scale)
+        for (b, h), (sel, _, _) in ref_sel.items():
+            n = int(cnt[b, h])
+            assert np.array_equal(idx[b, h, :n].cpu().numpy(), sel)
+            H.assert_close(out[b, h].cpu().numpy(), ref[(b, h)][0], "O")
+            H.assert_close(lse[b, h:h + 1].cpu().numpy(), np.array([ref[(b, h)][1]]), "lse")

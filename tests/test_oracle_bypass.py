@@ -109,3 +109,17 @@ def test_partition_covers_every_token_once():
         allt = np.concatenate([[0], glo, loc])
         assert np.array_equal(np.sort(allt), np.arange(L))
         assert len(loc) == min(6, L - 1)
+
+
+@pytest.mark.parametrize("L", [2, 3, 7, 64, 1000])
+def test_bypass_output_is_the_mean_over_all_L_rows(L):
+    # V row t = t e_0 (plus rows beyond L that must not count): the mean over
+    # rows 0..L-1 is (L-1)/2 e_0 by the arithmetic-series sum, so a mean over
+    # a shorter or shifted range, or one that includes a row past L, fails.
+    V = np.zeros((L + 5, D))
+    V[:, 0] = np.arange(L + 5, dtype=np.float64)
+    V[L:, 1] = 1e6
+    got = orc.bypass_output(V, L)
+    want = np.zeros(D)
+    want[0] = (L - 1) / 2.0
+    assert np.array_equal(got, want)

@@ -24,7 +24,7 @@ def _noalloc(prob, dev, idx, cnt, gran, status):
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     rc = sa.lib().sa_sparse_decode_noalloc(
         prob.ref, p(dev["q"]), p(dev["k_pool"]), p(dev["v_pool"]), p(dev["page_table"]), p(dev["seq_lens"]),
-        p(idx), p(cnt), gran, p(out), p(lse), None, p(status),
+        p(idx), p(cnt), gran, p(out), p(lse), None, None if status is None else p(status),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == sa.SA_OK, sa.status_string(rc)
     return out, lse
@@ -52,6 +52,40 @@ def test_noalloc_matches_workspace_decode_twice(name):
         H.assert_close(o.cpu().numpy(), ref_o.cpu().numpy(), "noalloc O")
         H.assert_close(l.cpu().numpy(), ref_l.cpu().numpy(), "noalloc lse")
         assert int(status.item()) == sa.SA_OK
+
+
+def _tiny_setup(seed):
+    wl = synth.workload("tiny_4k")
+    case = synth.make_decode_case(wl, seed)
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    dev = H.to_dev(case)
+    ws = sa.Workspace(prob)
+    summ = H.gpu_summaries(prob, dev, ws)
+    idx, cnt, _ = H.gpu_select(prob, dev, summ, ws, with_scores=False)
+    ref_o, ref_l = H.gpu_decode(prob, dev, idx, cnt, ws)
+    return prob, dev, idx, cnt, ref_o, ref_l
+
+
+def test_noalloc_without_a_status_word():
+    # status_or_null = NULL: the status lives in the library's scratch; the
+    # outputs are what counts
+    prob, dev, idx, cnt, ref_o, ref_l = _tiny_setup(22)
+    for _ in range(2):
+        o, l = _noalloc(prob, dev, idx, cnt, sa.SEL_BLOCK, None)
+        torch.cuda.synchronize()
+        H.assert_close(o.cpu().numpy(), ref_o.cpu().numpy(), "noalloc O (no status word)")
+        H.assert_close(l.cpu().numpy(), ref_l.cpu().numpy(), "noalloc lse (no status word)")
+
+
+def test_noalloc_clears_a_stale_status():
+    # a status word left holding an error code from earlier reads SA_OK after a clean call
+    prob, dev, idx, cnt, ref_o, ref_l = _tiny_setup(23)
+    status = torch.full((1,), sa.SA_ERR_TIMEOUT, dtype=torch.int32, device="cuda")
+    o, l = _noalloc(prob, dev, idx, cnt, sa.SEL_BLOCK, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == sa.SA_OK
+    H.assert_close(o.cpu().numpy(), ref_o.cpu().numpy(), "noalloc O")
 
 
 def test_noalloc_rejects_problem_larger_than_its_scratch():
