@@ -155,28 +155,44 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- our arm
 
+def unit_decode_bytes(L, S, W, Bs, P, D, G, sel_lists):
+    """Algorithmic bytes of the decode for one (sequence, KV head): the K and
+    V rows of I U (union over the group's heads of their selected blocks
+    inside M), read once per group, q, O + lse, one page-table entry per page."""
+    s_end = min(S, L)
+    w_beg = max(L - W, s_end)
+    att = np.zeros(max(L, 1), dtype=bool)
+    att[:s_end] = True
+    att[w_beg:L] = True
+    for ids in sel_lists:
+        ids = np.asarray(ids, dtype=np.int64)
+        if ids.size == 0:
+            continue
+        t = (ids[:, None] * Bs + np.arange(Bs)[None, :]).ravel()
+        t = t[(t >= s_end) & (t < w_beg)]
+        att[t] = True
+    att = att[:L]
+    ntok = int(att.sum())
+    npages = int(np.unique(np.nonzero(att)[0] // P).size)
+    return ntok * 2 * D * 2 + G * D * 2 + G * (D * 4 + 4) + npages * 4
+
+
 def algorithmic_bytes(wl, prob, seq_lens, sel_idx, sel_cnt):
     """Per-step algorithmic HBM bytes, split by call (byte accounting of the
     hot-path scope: summaries of candidate blocks, KV rows of I U (union of the
     group's selected blocks) once per group, q, O + lse, page-table entries)."""
     P, D, G = wl.P, wl.D, wl.G
-    si, sc = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
+    si = sel_idx.cpu().numpy() if hasattr(sel_idx, "cpu") else np.asarray(sel_idx)
+    sc = sel_cnt.cpu().numpy() if hasattr(sel_cnt, "cpu") else np.asarray(sel_cnt)
     dec = sel = summ = 0
+    summ_row = 2 * D * 2 if prob.mode == sa.SUMMARY_MINMAX else D * 2
     for b in range(wl.B):
         L = int(seq_lens[b])
-        s_end = min(wl.S, L)
-        w_beg = max(L - wl.W, s_end)
         for kvh in range(wl.Hk):
             Bs = wl.block_sizes[kvh]
             j0, j1 = synth.candidate_range(L, wl.S, wl.W, Bs)
-            toks = set(range(0, s_end)) | set(range(w_beg, L))
-            for g in range(G):
-                h = kvh * G + g
-                for j in si[b, h, :sc[b, h]]:
-                    toks.update(range(max(j * Bs, s_end), min((j + 1) * Bs, w_beg)))
-            pages = {t // P for t in toks}
-            dec += len(toks) * 2 * D * 2 + G * D * 2 + G * (D * 4 + 4) + len(pages) * 4
-            summ_row = 2 * D * 2 if prob.mode == sa.SUMMARY_MINMAX else D * 2
+            lists = [si[b, kvh * G + g, :sc[b, kvh * G + g]] for g in range(G)]
+            dec += unit_decode_bytes(L, wl.S, wl.W, Bs, P, D, G, lists)
             sel += (j1 - j0) * summ_row + G * D * 2 + G * 4 * (1 + int(np.mean(sc[b, kvh * G:(kvh + 1) * G])))
             summ += Bs * D * 2 + summ_row + ((Bs + P - 1) // P) * 4
     return {"decode": dec, "select": sel, "summary": summ, "total": dec + sel + summ}
@@ -280,24 +296,16 @@ def run_ours(args):
         g_group = capture(group_step)
         torch.cuda.synchronize()
 
-    def timed(g):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+    R = args.repeats
 
     with torch.cuda.stream(stream):   # warm-up steps, eager
         for i in range(W):
             sub_select(layers[i % N_LAYERS])
             sub_decode(layers[i % N_LAYERS])
-    timed(g_dec)                      # first replays upload the graphs
-    timed(g_sel)
-    timed(g_step)
+    for g in (g_dec, g_sel, g_step):  # first replays upload the graphs
+        replay_ms(g, stream, 1)
     if prob_g is not None:
-        timed(g_group)
+        replay_ms(g_group, stream, 1)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -305,22 +313,23 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
-    total_ms = timed(g_step)
-    dec_total = timed(g_dec)
-    sel_total = timed(g_sel)
+    # each graph replayed R times, every replay its own K-step timed window
+    step_reps = replay_ms(g_step, stream, R)
+    dec_reps = replay_ms(g_dec, stream, R)
+    sel_reps = replay_ms(g_sel, stream, R)
     group = None
     if prob_g is not None:
-        g_ms = timed(g_group) / K
+        g_sp = spread(replay_ms(g_group, stream, R), K)
+        g_ms = g_sp["median_ms_per_step"]
         g_bytes = float(np.mean([nbytes_g[(W + i) % N_LAYERS]["total"] for i in range(K)]))
         group = {"selection": "one top-k per KV head over the fp32 sum of its query heads' scores (a variant; "
                               "the headline selects per head)",
-                 "ms_per_step": round(g_ms, 5), "value": round(wl.B * wl.Hq / (g_ms / 1e3), 1),
+                 "ms_per_step": g_ms, "spread": g_sp, "value": round(wl.B * wl.Hq / (g_ms / 1e3), 1),
                  "unit": "queries/s", "algorithmic_bytes_per_step": int(g_bytes),
                  "achieved_gbs": round(g_bytes / (g_ms / 1e3) / 1e9, 1)}
     clk = clocks.stop()
-    dec_ms = [dec_total / K]
-    sel_ms = [sel_total / K]
-    total_ms = reduce_max_ms(total_ms, world, dev)
+    step_sp, dec_sp, sel_sp = spread(step_reps, K), spread(dec_reps, K), spread(sel_reps, K)
+    total_ms = reduce_max_ms(float(np.median(step_reps)), world, dev)   # median K-step window, slowest rank
     ms_step = total_ms / K
     queries = wl.B * wl.Hq
     value = whole_job_value(world, queries, K, total_ms)
@@ -328,7 +337,7 @@ def run_ours(args):
     layer_of = [(W + i) % N_LAYERS for i in range(K)]
     dec_bytes = float(np.mean([nbytes[l]["decode"] for l in layer_of]))
     step_bytes = float(np.mean([nbytes[l]["total"] for l in layer_of]))
-    dec_avg_ms = float(np.mean(dec_ms))
+    dec_avg_ms = dec_sp["median_ms_per_step"]
     peak, peak_src = measured_hbm_peak()
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
 
@@ -336,6 +345,7 @@ def run_ours(args):
     e2e = None if args.no_e2e else run_e2e(args, prob, layers, ws, out, lse, dev)
     tables = None if args.no_tables else run_tables(args, dev)
     bypass = None if args.no_bypass else run_bypass(args, dev, rank)
+    config2 = None if args.no_config2 else run_qwen(args, dev, rank)
     gpu_launches = STEP_LAUNCHES * K
 
     res = {
@@ -351,35 +361,68 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V with planted sink, heavy blocks and recency ramp)",
-        "config": {"workload": "llama3.1-8b layer, decode, B8 x 32q/8kv heads x D128, ctx 32768, "
-                               "page=block=16, budget 5% (k=100 blocks), sinks 4, window 1024, minmax summaries",
-                   "global_batch": wl.B, "seq_len": wl.L, "parallelism": f"replicas x{world}",
-                   "l2": f"{N_LAYERS} rotating independent layer copies ({N_LAYERS * 1.07:.1f} GB KV), inputs > L2"},
+        "config": headline_config(world),
+        "timing": {"method": f"CUDA events around each of {R} replays of one CUDA graph of K = {K} steps; "
+                             "value and ms_per_step from the median replay",
+                   "l2": f"{N_LAYERS} rotating independent layer copies ({N_LAYERS * 1.07:.1f} GB KV), inputs > L2",
+                   "repeats": R},
+        "spread": step_sp,
         "roofline": {"bound": "hbm", "kernel": "sa_sparse_decode (tile build + paged decode + split-K merge), timed alone",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
-                     "algorithmic_bytes_per_launch": int(dec_bytes), "avg_launch_ms": round(dec_avg_ms, 5)},
+                     "algorithmic_bytes_per_launch": int(dec_bytes), "avg_launch_ms": round(dec_avg_ms, 5),
+                     "spread": dec_sp},
         "step_roofline": {"achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
                           "frac": round(step_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
                           "algorithmic_bytes_per_step": int(step_bytes),
-                          "select_avg_ms": round(float(np.mean(sel_ms)), 5)},
+                          "select_avg_ms": sel_sp["median_ms_per_step"], "select_spread": sel_sp},
         "e2e": e2e,
         "tables_roofline": tables,
+        "config2": config2,
         "group_select_variant": group,
         "bypass_variant": bypass,
         "gpu_launches": gpu_launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(layers[0], wl, ks, prob.scale, budget_s=args.cpu_seconds)
-        cb.pop("queries")
-        res["cpu_baseline"] = cb
+        res["cpu_baseline"] = cpu_baseline_cells(args, dev, layers[0], wl, ks, prob.scale)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def headline_config(world):
+    """The workload the headline is quoted on (both arms print this)."""
+    wl = synth.workload(WORKLOAD)
+    return {"workload": "llama3.1-8b layer, decode, B8 x 32q/8kv heads x D128, ctx 32768, "
+                        "page=block=16, budget 5% (k=100 blocks), sinks 4, window 1024, minmax summaries",
+            "global_batch": wl.B, "seq_len": wl.L, "parallelism": f"replicas x{world}"}
+
+
+def replay_ms(g, stream, reps):
+    """Milliseconds of each of `reps` replays of graph g, CUDA events on the
+    launching stream, the device synchronised on both sides of every replay."""
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def spread(reps_ms, steps):
+    """Median, p10 and p90 of the per-step time over the replays."""
+    a = np.asarray(reps_ms, dtype=np.float64) / steps
+    return {"median_ms_per_step": round(float(np.median(a)), 5), "p10_ms_per_step": round(float(np.percentile(a, 10)), 5),
+            "p90_ms_per_step": round(float(np.percentile(a, 90)), 5), "repeats": int(a.size)}
 
 
 def run_e2e(args, prob, layers, ws, out, lse, dev):
@@ -513,15 +556,9 @@ def run_tables(args, dev, reps=100):
         with torch.cuda.graph(g, stream=st, capture_error_mode="relaxed"):
             for i in range(reps):
                 update(i)
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(st):
-        e0.record(st)
-        g.replay()
-        e1.record(st)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    replay_ms(g, st, 1)
+    tab_sp = spread(replay_ms(g, st, args.repeats), reps)
+    ms = tab_sp["median_ms_per_step"]
     status = ws.status()
     # algorithmic bytes: both tables read and written, the previous step's logits at
     # its attended positions, its selection list, and the new candidate list
@@ -544,14 +581,8 @@ def run_tables(args, dev, reps=100):
         with torch.cuda.graph(g2, stream=st, capture_error_mode="relaxed"):
             for i in range(reps):
                 sa.select_tokens(prob_t, q1, case.k_pool, case.page_table, sl1, cand[1], cnt[1], tsel, tcnt, ws)
-    g2.replay()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(st):
-        e0.record(st)
-        g2.replay()
-        e1.record(st)
-    torch.cuda.synchronize()
-    ms_tok = e0.elapsed_time(e1) / reps
+    replay_ms(g2, st, 1)
+    ms_tok = spread(replay_ms(g2, st, args.repeats), reps)["median_ms_per_step"]
     n_cand = cnt[1].sum().item()
     tok_bytes = n_cand * (wl.D * 2 + 4 + 4 + 4) + B * Hq * (wl.D * 2 + 16 * 4 + 8)
     token_topk = {"kernel": "sa_select_tokens (canonical q.k over each head's candidates, top 16)",
@@ -561,7 +592,7 @@ def run_tables(args, dev, reps=100):
                   "note": "a few KB a head: launch and latency bound, not bandwidth bound"}
     return {"workload": "score tables, B4 x 32q/8kv heads, L 131072 + 1, tables fp32 [4][32][131136] x2",
             "kernel": "sa_update_score_tables (decay, threshold, expansion in one pass)",
-            "avg_launch_ms": round(ms, 5), "algorithmic_bytes_per_launch": int(nbytes),
+            "avg_launch_ms": round(ms, 5), "spread": tab_sp, "algorithmic_bytes_per_launch": int(nbytes),
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "mean_candidates_per_head": round(cnt[1].float().mean().item(), 1), "status": status,
             "exact_token_topk": token_topk}
@@ -628,17 +659,11 @@ def run_bypass(args, dev, rank, reps=200):
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
                 for i in range(reps):
                     fn(layers[i % N_LAYERS])
-        g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        replay_ms(g, stream, 1)
+        sp = spread(replay_ms(g, stream, max(5, args.repeats // 3)), reps)
+        ms = sp["median_ms_per_step"]
         b = float(np.mean([nbytes[i % N_LAYERS] for i in range(reps)]))
-        res[name] = {"ms_per_step": round(ms, 5), "value": round(wl.B * wl.Hq / (ms / 1e3), 1),
+        res[name] = {"ms_per_step": round(ms, 5), "spread": sp, "value": round(wl.B * wl.Hq / (ms / 1e3), 1),
                      "unit": "queries/s", "algorithmic_bytes_per_step": int(b),
                      "achieved_gbs": round(b / (ms / 1e3) / 1e9, 1)}
         del g
@@ -750,60 +775,216 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def run_qwen(args, dev, rank, n_layers=4):
+    """Config 2: the Qwen2.5-7B-shaped layer with head-specific granularity
+    and budget (B16, 28 q / 4 KV heads, G = 7, ctx 65536, block size per KV
+    head from {8, 16, 32, 64}, budget per KV head in [2 %, 20 %]; Fluxion core
+    claim and Fig. 5): the whole step (sa_decode_step), `n_layers`
+    independent layer copies (2.15 GB of KV each) rotating, a CUDA graph of K
+    steps replayed R times."""
+    wl = synth.workload("qwen_64k")
+    ks = synth.k_per_qhead(wl)
+    kcap = max(ks)
+    prob = sa.Problem(B=wl.B, Hq=wl.Hq, Hk=wl.Hk, max_pages_per_seq=wl.max_pages_per_seq,
+                      num_pages=wl.B * wl.max_pages_per_seq, sink=wl.S, window=wl.W,
+                      block_sizes=wl.block_sizes, k_per_head=ks, kcap=kcap, mode=sa.SUMMARY_MINMAX)
+    ws = sa.Workspace(prob, device=dev)
+    layers = []
+    for l in range(n_layers):
+        c = synth.make_decode_case(wl, 1000 * rank + 2000 + l, device=dev)
+        summ = torch.empty(prob.summary_shape(), dtype=torch.bfloat16, device=dev)
+        sa.block_summarize(prob, c.k_pool, c.page_table, c.seq_lens, summ, ws)
+        layers.append(dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens, summ=summ,
+                           sel_idx=torch.empty(wl.B, wl.Hq, kcap, dtype=torch.int32, device=dev),
+                           sel_cnt=torch.empty(wl.B, wl.Hq, dtype=torch.int32, device=dev)))
+        del c
+    out = torch.empty(wl.B, wl.Hq, wl.D, device=dev)
+    lse = torch.empty(wl.B, wl.Hq, device=dev)
+
+    def step(L):
+        sa.decode_step(prob, L["q"], L["k"], L["v"], L["pt"], L["sl"], L["summ"], L["sel_idx"], L["sel_cnt"], out,
+                       lse, ws)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for L in layers:
+            step(L)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    nbytes = [algorithmic_bytes(wl, prob, L["sl"].cpu().numpy(), L["sel_idx"], L["sel_cnt"])["total"]
+              for L in layers]
+    K, W = args.steps, args.warmup
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(layers[i % n_layers])
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for i in range(K):
+                step(layers[(W + i) % n_layers])
+    replay_ms(g, stream, 1)
+    sp = spread(replay_ms(g, stream, args.repeats), K)
+    ms = sp["median_ms_per_step"]
+    b = float(np.mean([nbytes[(W + i) % n_layers] for i in range(K)]))
+    peak, _ = measured_hbm_peak()
+    achieved = b / (ms / 1e3) / 1e9
+    assert ws.status() == sa.SA_OK
+    del g, layers, ws
+    torch.cuda.empty_cache()
+    return {"workload": "qwen2.5-7b layer, decode, B16 x 28q/4kv heads (G 7) x D128, ctx 65536, block size per KV "
+                        f"head {wl.block_sizes}, budget per KV head {[bp / 100 for bp in wl.budget_bp]} %, sinks 4, "
+                        "window 1024, minmax summaries",
+            "call": "sa_decode_step", "ms_per_step": ms, "spread": sp,
+            "value": round(wl.B * wl.Hq / (ms / 1e3), 1), "unit": "queries/s",
+            "algorithmic_bytes_per_step": int(b), "achieved": round(achieved, 1), "peak": peak, "unit_bw": "GB/s",
+            "frac": round(achieved / peak, 4), "l2": f"{n_layers} rotating layer copies ({n_layers * 2.15:.1f} GB KV)"}
+
+
 # --------------------------------------------------------------------------- oracle timing
 
-def cpu_baseline(L, wl, ks, scale, budget_s=15.0, units=None):
-    """Time the fp64 oracle (as it stands) on a bounded sample of the same
-    workload: selection + decode for whole (sequence, KV head) units."""
-    from oracle import sparse_attention_oracle as orc
-    from tests import harness as H
+def _bits(t):
+    """bf16 tensor -> numpy uint16 bits on the host."""
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
-    nc = H.NpCase(q=orc.to_np(L["q"]), k_pool=orc.to_np(L["k"]), v_pool=orc.to_np(L["v"]),
-                  page_table=orc.to_np(L["pt"]), seq_lens=orc.to_np(L["sl"]))
-    all_units = [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
-    done = 0
-    t0 = time.perf_counter()
-    for u in (units or all_units):
-        sel = H.oracle_select(nc, wl, ks, "minmax", units=[u])
-        H.oracle_decode(nc, wl, {k: v[0] for k, v in sel.items()}, sa.SEL_BLOCK, scale, units=[u])
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    q = done * wl.G
-    return {"value": round(q / dt, 2), "unit": "queries/s", "cores": 1, "kind": "oracle", "queries": q,
-            "sample": f"{done} of {len(all_units)} (sequence, KV head) units = {q} queries of one layer "
-                      f"step (summaries + canonical scores + top-k + fp64 attention + merge), {dt:.1f} s"}
+
+def _cell(name, unit, queries_per_step, secs_per_step, cores, sample, extrapolated):
+    return {"cell": name, "value": round(queries_per_step / secs_per_step, 2), "unit": unit, "cores": cores,
+            "s_per_step": round(secs_per_step, 4), "sample": sample, "extrapolated": extrapolated}
+
+
+def _decode_cells(OT, pool, name, case_q, case_k, case_v, pt, lens, wl, ks, scale, budget_s, units=None,
+                  total_units=None):
+    """The oracle on one block-selection step of a case: one core (a bounded
+    run over the units, scaled to the whole step when cut short) and all
+    cores (every unit, or the sample `units` scaled to `total_units`)."""
+    sp = OT.SharedPools(_bits(case_k), _bits(case_v))
+    try:
+        jobs = OT.decode_jobs(sp.spec(), case_q.float().cpu().numpy(), pt.cpu().numpy(), [int(x) for x in lens],
+                              wl.block_sizes, ks, wl.S, wl.W, "minmax", scale, units=units)
+        n_all = total_units or len(jobs)
+        queries = wl.B * wl.Hq
+        t1, n1 = OT.time_serial(jobs, sp.local, budget_s)
+        one = _cell(name, "queries/s", queries, t1 / n1 * n_all, 1,
+                    f"{n1} of {n_all} (sequence, KV head) units in {t1:.2f} s", n1 < n_all)
+        tn = OT.time_parallel(pool, jobs)
+        many = _cell(name, "queries/s", queries, tn * n_all / len(jobs), pool.cores,
+                     f"{len(jobs)} of {n_all} units over {pool.cores} worker processes in {tn:.2f} s",
+                     len(jobs) < n_all)
+        return [one, many]
+    finally:
+        sp.close()
+
+
+def cpu_baseline_cells(args, dev, L0, wl, ks, scale):
+    """The oracle as it stands, timed on this machine's host cores on one
+    core and on all of them (a spawn-started process pool over units), for
+    the workloads of the hot path: the 4K tiny case, the 32K Llama layer
+    (the headline), the 64K Qwen layer (a sampled slice, extrapolated), the
+    128K score-table step (plus its 64-step total, extrapolated) and the
+    batch-1 8K / 32K layers of the stack sweep."""
+    from tests import oracle_timing as OT
+
+    budget = max(2.0, args.cpu_seconds)
+    pool = OT.OraclePool()
+    cells = []
+    try:
+        # config 1: layer 0 of the headline run
+        c1 = _decode_cells(OT, pool, "llama_32k: B8 x 32q/8kv, ctx 32768, 5 %", L0["q"], L0["k"], L0["v"], L0["pt"],
+                           L0["sl"].tolist(), wl, ks, scale, budget * 0.4)
+        cells += c1
+        # config 0
+        w0 = synth.workload("tiny_4k")
+        c = synth.make_decode_case(w0, 0, device=dev)
+        cells += _decode_cells(OT, pool, "tiny_4k: B1 x 8q/2kv, ctx 4096, 10 %", c.q, c.k_pool, c.v_pool,
+                               c.page_table, c.seq_lens.tolist(), w0, synth.k_per_qhead(w0), scale, budget * 0.05)
+        # config 4: batch-1 cells of the sweep, one layer, 5 % budget
+        for ctx in (8192, 32768):
+            w4 = synth.sweep_workload(1, ctx, 500, extra_tokens=0)
+            c = synth.make_decode_case(w4, 7000, device=dev)
+            cells += _decode_cells(OT, pool, f"stack sweep cell: B1 x 32q/8kv, ctx {ctx}, 5 %, one layer", c.q,
+                                   c.k_pool, c.v_pool, c.page_table, c.seq_lens.tolist(), w4,
+                                   synth.k_per_qhead(w4), scale, budget * 0.05)
+        # config 2: one unit per KV head on one core, 16 units over the pool; scaled to the 64 units
+        w2 = synth.workload("qwen_64k")
+        c = synth.make_decode_case(w2, 2000, device=dev)
+        units = [(b, kvh) for b in range(w2.B) for kvh in range(w2.Hk)][::4]
+        cells += _decode_cells(OT, pool, "qwen_64k: B16 x 28q/4kv, ctx 65536, per-KV-head Bs and budget", c.q,
+                               c.k_pool, c.v_pool, c.page_table, c.seq_lens.tolist(), w2, synth.k_per_qhead(w2),
+                               scale, budget * 0.15, units=units, total_units=w2.B * w2.Hk)
+        del c
+        # config 3: one score-table step, every head; the 64-step total scaled from it
+        w3 = synth.table_workload("tables_128k")
+        tc = synth.make_table_case(w3, 7, device=dev)
+        sp = OT.SharedPools(_bits(tc.k_pool), _bits(tc.v_pool))
+        try:
+            heads = [(b, h) for b in range(w3.B) for h in range(w3.Hq)]
+            jobs = OT.table_jobs(sp.spec(), tc.q_steps[0].float().cpu().numpy(), tc.q_steps[1].float().cpu().numpy(),
+                                 tc.page_table.cpu().numpy(), tc.vert0.cpu().numpy(), tc.slash0.cpu().numpy(), w3.L0,
+                                 w3.S, w3.W, w3.beta, w3.kcap, w3.G, scale, heads)
+            t1, n1 = OT.time_serial(jobs, sp.local, budget * 0.3)
+            q3 = w3.B * w3.Hq
+            name = "tables_128k: B4 x 32q/8kv, ctx 131072 + 1, score-table step"
+            one = _cell(name, "queries/s", q3, t1 / n1 * len(jobs), 1, f"{n1} of {len(jobs)} heads in {t1:.2f} s",
+                        n1 < len(jobs))
+            tn = OT.time_parallel(pool, jobs)
+            many = _cell(name, "queries/s", q3, tn, pool.cores, f"{len(jobs)} heads over {pool.cores} workers", False)
+            for cc in (one, many):
+                cc["s_per_64_steps"] = round(cc["s_per_step"] * w3.steps, 2)
+                cc["s_per_64_steps_extrapolated"] = True
+            cells += [one, many]
+        finally:
+            sp.close()
+        del tc
+        torch.cuda.empty_cache()
+    finally:
+        pool.close()
+    head = c1[1]
+    return {"value": head["value"], "unit": "queries/s", "cores": head["cores"], "kind": "oracle",
+            "sample": f"llama_32k step, {head['sample']}; one core: {c1[0]['value']} queries/s ({c1[0]['sample']})",
+            "cells": cells}
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands on this machine's host
+    cores (a spawn-started process pool over the (sequence, KV head) units),
+    one whole 32K Llama-layer step per timed step; inputs generated on the
+    host, no GPU."""
     world, rank, local = dist_info()
     if rank != 0:
         return
+    from tests import oracle_timing as OT
+
     wl = synth.workload(WORKLOAD)
     ks = synth.k_per_qhead(wl)
     c = synth.make_decode_case(wl, 100)
-    L = dict(q=c.q, k=c.k_pool, v=c.v_pool, pt=c.page_table, sl=c.seq_lens)
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    units = [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hk)]
-    for i in range(args.warmup):
-        cpu_baseline(L, wl, ks, 1 / math.sqrt(wl.D), budget_s=0.0, units=units[i % len(units):][:1])
-    t0 = time.perf_counter()
-    nq = 0
-    for i in range(args.steps):
-        r = cpu_baseline(L, wl, ks, 1 / math.sqrt(wl.D), budget_s=per_step, units=units)
-        nq += r["queries"]
-    dt = time.perf_counter() - t0
+    sp = OT.SharedPools(_bits(c.k_pool), _bits(c.v_pool))
+    pool = OT.OraclePool()
+    try:
+        jobs = OT.decode_jobs(sp.spec(), c.q.float().numpy(), c.page_table.numpy(), c.seq_lens.tolist(),
+                              wl.block_sizes, ks, wl.S, wl.W, "minmax", 1 / math.sqrt(wl.D))
+        # a step is the whole layer step when the pool can do it in about a second, else a bounded
+        # sample of its units (scaled to queries of the units done)
+        per_step = max(1, min(len(jobs), int(len(jobs) * pool.cores / 16)))
+        for i in range(args.warmup):
+            OT.time_parallel(pool, jobs[:pool.cores])
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            OT.time_parallel(pool, jobs[:per_step])
+        dt = time.perf_counter() - t0
+    finally:
+        pool.close()
+        sp.close()
+    nq = per_step * wl.G * args.steps
     v = round(nq / dt, 2)
+    sample = (f"{per_step} of {len(jobs)} (sequence, KV head) units of one 32K Llama-layer step per timed step "
+              f"(summaries + canonical scores + top-k + fp64 attention + merge), {args.steps} steps, "
+              f"{pool.cores} worker processes")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "llama3.1-8b layer, decode, B8 x 32q/8kv, ctx 32768, 5% budget",
-                                        "global_batch": wl.B, "seq_len": wl.L, "parallelism": "cpu oracle"},
-        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{nq} queries over {args.steps} steps, each a bounded sample of (sequence, KV "
-                                   f"head) units of one layer step"},
+        "data": "synthetic (seeded N(0,1) Q/K/V with planted sink, heavy blocks and recency ramp)",
+        "config": headline_config(world),
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": pool.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -822,6 +1003,8 @@ def main():
     ap.add_argument("--no-tables", action="store_true", help="skip the score-table (a7) leg")
     ap.add_argument("--no-group", action="store_true", help="skip the group-shared selection variant")
     ap.add_argument("--no-bypass", action="store_true", help="skip the head-sparsity bypass variant")
+    ap.add_argument("--no-config2", action="store_true", help="skip the Qwen-shaped 64K leg (config 2)")
+    ap.add_argument("--repeats", type=int, default=30, help="replays of each timed CUDA graph (median, p10, p90)")
     ap.add_argument("--sweep", action="store_true",
                     help="the batch x context x budget throughput sweep of a 32-layer stack (one line per cell)")
     ap.add_argument("--sweep-cells", default="",

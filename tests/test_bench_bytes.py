@@ -5,6 +5,7 @@ of I and J_h (read once per group), q, O + lse, and one page-table entry per
 page read; the selection reads each candidate block's summary once per group.
 CPU only."""
 import numpy as np
+import pytest
 import torch
 
 import bench
@@ -28,8 +29,13 @@ def _count(wl, nc, sel):
     return dec
 
 
-def test_decode_bytes_match_an_independent_count():
-    wl = synth.workload("tiny_4k")
+@pytest.mark.parametrize("name", ["tiny_4k", "ragged"])
+def test_decode_bytes_match_an_independent_count(name):
+    if name == "tiny_4k":
+        wl = synth.workload("tiny_4k")
+    else:   # block sizes 8 and 64 (half a page, four pages), ragged lengths
+        wl = synth.Workload("ragged", B=3, Hq=6, Hk=2, L=1500, block_sizes=[8, 64], budget_bp=[1500, 800],
+                            S=4, W=96, c_heavy=2.0, heavy_count=4, recency=300, lens=[1500, 1013, 333])
     case = synth.make_decode_case(wl, 2)
     nc = H.to_np_case(case)
     ks = synth.k_per_qhead(wl)
@@ -44,7 +50,10 @@ def test_decode_bytes_match_an_independent_count():
     got = bench.algorithmic_bytes(wl, prob, nc.seq_lens, idx, cnt)
     assert got["decode"] == _count(wl, nc, sel)
     # selection: every candidate block's MINMAX summary (2 x D bf16) read once per group
-    L = int(nc.seq_lens[0])
-    j0, j1 = orc.candidate_blocks(L, wl.S, wl.W, wl.block_sizes[0])
-    assert got["select"] >= wl.B * wl.Hk * (j1 - j0) * 2 * wl.D * 2
+    ncand = 0
+    for b in range(wl.B):
+        for kvh in range(wl.Hk):
+            j0, j1 = orc.candidate_blocks(int(nc.seq_lens[b]), wl.S, wl.W, wl.block_sizes[kvh])
+            ncand += j1 - j0
+    assert got["select"] >= ncand * 2 * wl.D * 2
     assert got["total"] == got["decode"] + got["select"] + got["summary"]
