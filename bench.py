@@ -906,7 +906,7 @@ def cpu_baseline_cells(args, dev, L0, wl, ks, scale):
         # config 2: one unit per KV head on one core, 16 units over the pool; scaled to the 64 units
         w2 = synth.workload("qwen_64k")
         c = synth.make_decode_case(w2, 2000, device=dev)
-        units = [(b, kvh) for b in range(w2.B) for kvh in range(w2.Hk)][::4]
+        units = [(b, b % w2.Hk) for b in range(w2.B)]   # every KV head (block size, budget) four times
         cells += _decode_cells(OT, pool, "qwen_64k: B16 x 28q/4kv, ctx 65536, per-KV-head Bs and budget", c.q,
                                c.k_pool, c.v_pool, c.page_table, c.seq_lens.tolist(), w2, synth.k_per_qhead(w2),
                                scale, budget * 0.15, units=units, total_units=w2.B * w2.Hk)

@@ -125,8 +125,6 @@ __device__ __forceinline__ int unit_of(const int* prefix, int U, long long x) {
   return lo;
 }
 
-// Floats per chunk partial: O[G][kD], then max[G] and sum[G], padded to 16 bytes.
-__host__ __device__ __forceinline__ int partial_stride(int G) { return (G * (kD + 2) + 3) & ~3; }
 
 __device__ __forceinline__ int ld_volatile(const int* x) { return *reinterpret_cast<const volatile int*>(x); }
 // CTA-scope acquire load / release store (ordering the chunk ring between

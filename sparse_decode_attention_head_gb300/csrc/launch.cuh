@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 
+#include "persist.cuh"
 #include "sa_common.cuh"
 #include "sparsity.cuh"
 #include "tables.cuh"

@@ -43,6 +43,10 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, SA_OK, code);
 }
 
+// Floats per chunk partial of a split-K decode: O[G][kD], then max[G] and
+// sum[G], padded to 16 bytes.
+__host__ __device__ __forceinline__ int partial_stride(int G) { return (G * (kD + 2) + 3) & ~3; }
+
 // Dense set I = [0, s_end) U [w_beg, L), middle region M = [s_end, w_beg).
 __host__ __device__ __forceinline__ void partition(int L, int S, int W, int& s_end, int& w_beg) {
   s_end = L < S ? L : S;
@@ -131,6 +135,25 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// GPU-scope acquire load / release store (cross-CTA hand-offs through global memory)
+__device__ __forceinline__ int ld_acquire_gpu(const int* x) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* x, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
+}
+// CTA-scope acquire load / release store (hand-offs between warps through shared memory)
+__device__ __forceinline__ int ld_acquire_block(const int* x) {
+  int v;
+  asm volatile("ld.acquire.cta.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_block(int* x, int v) {
+  asm volatile("st.release.cta.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- mbarrier / TMA
