@@ -60,6 +60,7 @@ constexpr int kBoxB = 16 * 64 * 2;               // one TMA box: 16 rows x 64 bf
 constexpr int kPRing = 3;                        // chunk ring entries
 constexpr int kFifo = 8;                         // per-warp issued-entry ring (slots + park markers)
 constexpr int kQOff = 6144;                      // score item: q rows at this offset of the slot
+constexpr int kItemBatch = 2;                    // score items a warp claims per ticket (one atomic)
 constexpr int kPartF = kD + 2;                   // floats per head in a parked state: O, max, sum
 constexpr int kBuildWin = 1024;                  // pages per tile-builder window
 constexpr int kHbWords = 64;                     // block-bitmap words per head and window (2048 blocks)
@@ -142,10 +143,14 @@ __device__ __forceinline__ uint32_t spread4(uint32_t n) {
   return (n & 1u) | ((n & 2u) << 7) | ((n & 4u) << 14) | ((n & 8u) << 21);
 }
 
-// Bounded poll (one lane) until *x >= v (GPU-scope acquire).  False on timeout.
+// Bounded poll (one lane) until *x >= v: relaxed loads, then one acquire
+// fence once the value is seen.  False on timeout.
 __device__ __forceinline__ bool wait_ge_gpu(const int* x, int v) {
   for (uint32_t i = 0; i < kSpinGlobal; ++i) {
-    if (ld_acquire_gpu(x) >= v) return true;
+    if (ld_relaxed_gpu(x) >= v) {
+      fence_acq_rel_gpu();
+      return true;
+    }
     __nanosleep(64);
   }
   return false;
@@ -276,13 +281,18 @@ __device__ __forceinline__ void attend_tile(const uint8_t* slot, const Tile& t, 
 
 // ------------------------------------------------------------------ merge of a unit's chunk partials
 
-// One warp: the exact merge of the nch partials of unit u (HGCA's fusion
-// identity over a chain, stabilised by the maximum); lane owns dims [4 lane, 4 lane + 4).
-__device__ void merge_unit_warp(const Params& p, const PArgs& A, int u, int pos0, int nch, int lane) {
+// The 128 selector threads: the exact merge of the nch partials of unit u
+// (HGCA's fusion identity over a chain, stabilised by the maximum).  Warp w
+// merges heads w, w + 4; lane j holds chunk j's (max, sum) (32 chunks at a
+// time), the weights e^{m_j - M} go round by shuffles, and the O rows (lane
+// owns dims [4 lane, 4 lane + 4)) are loaded eight chunks at a time, so the
+// L2 round trips overlap.
+__device__ void merge_unit(const Params& p, const PArgs& A, int u, int pos0, int nch) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int G = p.G, PS = partial_stride(G);
   const float* P = A.partials + (size_t)pos0 * PS;
   const int b = u / p.Hk, kvh = u % p.Hk;
-  for (int g = 0; g < G; ++g) {
+  for (int g = w; g < G; g += kPSel) {
     float M = -INFINITY;
     for (int j = lane; j < nch; j += 32) M = fmaxf(M, __ldcg(P + (size_t)j * PS + G * kD + g));
 #pragma unroll
@@ -290,16 +300,34 @@ __device__ void merge_unit_warp(const Params& p, const PArgs& A, int u, int pos0
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
     if (M != -INFINITY) {
-      for (int j = 0; j < nch; ++j) {
-        const float* pc = P + (size_t)j * PS;
-        const float mj = __ldcg(pc + G * kD + g);
-        const float f = mj == -INFINITY ? 0.f : exp2f(mj - M);
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(pc + g * kD) + lane);
-        acc.x += f * x.x;
-        acc.y += f * x.y;
-        acc.z += f * x.z;
-        acc.w += f * x.w;
-        l += f * __ldcg(pc + G * kD + G + g);
+      for (int j0 = 0; j0 < nch; j0 += 32) {
+        const int j = j0 + lane;
+        float mj = -INFINITY, lj = 0.f;
+        if (j < nch) {
+          mj = __ldcg(P + (size_t)j * PS + G * kD + g);
+          lj = __ldcg(P + (size_t)j * PS + G * kD + G + g);
+        }
+        const float fj = mj == -INFINITY ? 0.f : exp2f(mj - M);
+        float lw = fj * lj;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+        l += lw;
+        const int nb = min(32, nch - j0);
+        for (int c0 = 0; c0 < nb; c0 += 8) {
+          float4 x[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            x[c] = c0 + c < nb ? __ldcg(reinterpret_cast<const float4*>(P + (size_t)(j0 + c0 + c) * PS + g * kD) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float f = __shfl_sync(0xffffffffu, fj, (c0 + c) & 31);
+            acc.x += f * x[c].x;
+            acc.y += f * x[c].y;
+            acc.z += f * x[c].z;
+            acc.w += f * x[c].w;
+          }
+        }
       }
     }
     const size_t row = (size_t)b * p.Hq + kvh * G + g;
@@ -312,13 +340,14 @@ __device__ void merge_unit_warp(const Params& p, const PArgs& A, int u, int pos0
 // ------------------------------------------------------------------ selector: tile list of a unit
 
 // The 128 selector threads: tiles of unit u from the G heads' selections (block
-// ids, global memory), page by page in windows of kBuildWin pages: a bit per
-// selected block per head, then per page the 16 per-token head masks (dense
-// tokens for every head, selected tokens inside M for their heads), a scan of
-// the touched pages and one 32-byte descriptor per tile.  Returns the tile
-// count (valid in every selector thread).
+// ids, global memory), in windows of kBuildWin pages.  Per window: a bit per
+// selected block per head; then per 32-page word the pages to read (pages
+// with dense-set tokens, and pages of selected blocks -- every such page holds
+// a token of M or of the dense set); a prefix of their counts; and one
+// 32-byte descriptor per touched page with its 16 per-token head masks.
+// Returns the tile count (valid in every selector thread).
 __device__ int build_unit(const Params& p, const PArgs& A, const Smem& S, int u) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int G = p.G;
   const int b = u / p.Hk, kvh = u % p.Hk;
   const int Lc = max(0, min(__ldg(A.seq_lens + b), p.mpp * kP));
@@ -333,7 +362,13 @@ __device__ int build_unit(const Params& p, const PArgs& A, const Smem& S, int u)
   const int* cnt_row = A.sel_cnt + h0;
   const int* pt_row = A.page_table + (size_t)b * p.mpp;
   Tile* T = A.tiles + (size_t)u * p.mpp;
-  int* scan = S.misc + M_SCAN;
+  uint32_t* touched = S.topk->cand;                             // [32] page words of the window
+  int* wpre = S.topk->hist;                                     // [33] tiles before word w; [32] = window total
+  // pages holding dense-set tokens: [0, ceil(s_end / P)) and [w_beg / P, npg)
+  const int d_lo_end = (s_end + kP - 1) / kP, d_hi_beg = w_beg / kP;
+  int* cnt_s = wpre + 40;   // [G] the heads' list lengths (hist[40 ..])
+  if (tid < G) cnt_s[tid] = max(0, min(__ldcg(cnt_row + tid), p.kcap));
+  sel_sync();
   int total = 0;
   for (int p0 = 0; p0 < npg; p0 += kBuildWin) {
     const int pw = min(kBuildWin, npg - p0);
@@ -341,88 +376,119 @@ __device__ int build_unit(const Params& p, const PArgs& A, const Smem& S, int u)
     const int nbw = ((pw * kP) + Bs - 1) >> lgB;              // blocks touching the window (<= 2048)
     for (int i = tid; i < G * kHbWords; i += kSelThreads) S.hb[i] = 0u;
     sel_sync();
-    for (int it = tid; it < G * p.kcap; it += kSelThreads) {
-      const int g = it / p.kcap, i = it - g * p.kcap;
-      const int cnt = min(__ldcg(cnt_row + g), p.kcap);
-      if (i >= cnt) continue;
-      const int x = __ldcg(sel_row + it) - blk0;
-      if (x < 0 || x >= nbw) continue;
-      atomicOr(&S.hb[g * kHbWords + (x >> 5)], 1u << (x & 31));
+    for (int it0 = 0; it0 < G * p.kcap; it0 += 4 * kSelThreads) {   // four list entries in flight a thread
+      int xv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int it = it0 + r * kSelThreads + tid;
+        const int g = it / p.kcap;
+        xv[r] = (it < G * p.kcap && it - g * p.kcap < cnt_s[g]) ? __ldcg(sel_row + it) : -1;
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int it = it0 + r * kSelThreads + tid;
+        const int x = xv[r] - blk0;
+        if (xv[r] < 0 || x < 0 || x >= nbw) continue;
+        atomicOr(&S.hb[(it / p.kcap) * kHbWords + (x >> 5)], 1u << (x & 31));
+      }
     }
     sel_sync();
-    // thread t: pages [8t, 8t + 8) of the window; masks computed twice (count, then write)
-    auto page_masks = [&](int pg, uint32_t (&m)[4]) {
-      const int tok0 = pg * kP;
-      uint32_t inM = 0u, dense = 0u;
+    if (tid < 32) {   // word tid: pages p0 + 32 tid .. + 31
+      const int q0 = 32 * tid;
+      uint32_t sel = 0u;
+      for (int g = 0; g < G; ++g) {
+        const uint32_t* hb = S.hb + g * kHbWords;
+        if (Bs == 16) {
+          sel |= hb[tid];
+        } else if (Bs == 8) {   // page x: blocks 2x, 2x + 1
+          const uint64_t w2 = ((uint64_t)hb[2 * tid + 1] << 32) | hb[2 * tid];
+          uint32_t v = 0u;
 #pragma unroll
-      for (int r = 0; r < kP; ++r) {
-        const int t = tok0 + r;
-        if (t < Lc) {
-          if (t >= s_end && t < w_beg) inM |= 1u << r; else dense |= 1u << r;
+          for (int i = 0; i < 32; ++i) v |= (uint32_t)(((w2 >> (2 * i)) & 3ull) != 0ull) << i;
+          sel |= v;
+        } else {   // Bs = 32 / 64: page x lies in block x >> (lgB - 4)
+          const int sh = lgB - 4;
+          const int jb = q0 >> sh;
+          const uint32_t bits = hb[jb >> 5] >> (jb & 31);
+          uint32_t v = 0u;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v |= ((bits >> (i >> sh)) & 1u) << i;
+          sel |= v;
         }
       }
-      uint32_t sel[kMaxG];
-      const int x = pg - p0;   // page within the window
+      // dense pages of this word
+      const int a = p0 + q0;
+      auto range_bits = [&](int lo, int hi) -> uint32_t {   // pages [lo, hi) within [a, a + 32)
+        lo = max(lo, a) - a;
+        hi = min(hi, a + 32) - a;
+        if (lo >= hi) return 0u;
+        const uint32_t up = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+        return up & ~((1u << lo) - 1u);
+      };
+      uint32_t t = (sel | range_bits(0, d_lo_end) | range_bits(d_hi_beg, npg)) & range_bits(p0, p0 + pw);
+      touched[tid] = t;
+      const int c = __popc(t);
+      const int incl = warp_incl_scan(c);
+      wpre[tid] = incl - c;
+      if (tid == 31) wpre[32] = incl;
+    }
+    sel_sync();
+    {   // thread t: word t >> 2, pages 8 (t & 3) .. + 7 of it
+      const int wd = tid >> 2, qb = (tid & 3) * 8;
+      const uint32_t tw = touched[wd];
+      uint32_t mine = (tw >> qb) & 0xffu;
+      int idx = total + wpre[wd] + __popc(tw & ((1u << qb) - 1u));
+      int ph[8];
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
-        uint32_t tm = 0u;
-        if (g < G && inM) {
-          const uint32_t* hb = S.hb + g * kHbWords;
-          if (Bs == 8) {
-            const int j = 2 * x;   // blocks 2x (rows 0-7) and 2x + 1 (rows 8-15) of the window
-            const uint32_t bits = (hb[j >> 5] >> (j & 31)) & 3u;
-            tm = ((bits & 1u) ? 0x00ffu : 0u) | ((bits & 2u) ? 0xff00u : 0u);
-          } else {
-            const int j = (x * kP + (p0 * kP - (blk0 << lgB))) >> lgB;
-            tm = ((hb[j >> 5] >> (j & 31)) & 1u) ? 0xffffu : 0u;
+      for (int i = 0; i < 8; ++i) ph[i] = ((mine >> i) & 1u) ? __ldg(pt_row + p0 + 32 * wd + qb + i) : -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!((mine >> i) & 1u)) continue;
+        const int x = 32 * wd + qb + i;   // page within the window
+        const int lp = p0 + x;
+        const int tok0 = lp * kP;
+        auto rng = [](int lo, int hi) -> uint32_t {   // token bits [lo, hi) of the page
+          lo = min(max(lo, 0), kP);
+          hi = min(max(hi, 0), kP);
+          return lo < hi ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
+        };
+        const uint32_t inM = rng(s_end - tok0, w_beg - tok0);
+        const uint32_t dense = rng(0, Lc - tok0) & ~inM;
+        uint32_t h_lo = 0u, h_hi = 0u;   // heads selecting rows 0-7 / 8-15 of the page
+        if (inM != 0u) {
+          for (int g = 0; g < G; ++g) {
+            const uint32_t* hb = S.hb + g * kHbWords;
+            if (Bs == 8) {
+              const int j = 2 * x;
+              const uint32_t bits = (hb[j >> 5] >> (j & 31)) & 3u;
+              h_lo |= (bits & 1u) << g;
+              h_hi |= ((bits >> 1) & 1u) << g;
+            } else {
+              const int j = (x * kP) >> lgB;
+              const uint32_t bit = (hb[j >> 5] >> (j & 31)) & 1u;
+              h_lo |= bit << g;
+              h_hi |= bit << g;
+            }
           }
-          tm &= inM;
         }
-        sel[g] = tm;
-      }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t v = spread4((dense >> (4 * q4)) & 15u) * all;
-#pragma unroll
-        for (int g = 0; g < kMaxG; ++g) v |= spread4((sel[g] >> (4 * q4)) & 15u) << g;
-        m[q4] = v;
-      }
-    };
-    int c = 0;
-    for (int r = 0; r < kBuildWin / kSelThreads; ++r) {
-      const int x = tid * (kBuildWin / kSelThreads) + r;
-      if (x < pw) {
         uint32_t m[4];
-        page_masks(p0 + x, m);
-        c += (m[0] | m[1] | m[2] | m[3]) != 0u;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t hsel = q4 < 2 ? h_lo : h_hi;
+          m[q4] = spread4((dense >> (4 * q4)) & 15u) * all | spread4((inM >> (4 * q4)) & 15u) * hsel;
+        }
+        const bool ok = ph[i] >= 0 && ph[i] < p.num_pages;
+        if (!ok) set_status(A.status, SA_ERR_BAD_PAGE);
+        int4* dst = reinterpret_cast<int4*>(T + idx);
+        dst[0] = make_int4(lp, ok ? ph[i] : -1, 0, 0);
+        dst[1] = make_int4((int)m[0], (int)m[1], (int)m[2], (int)m[3]);
+        ++idx;
       }
     }
-    const int xs = warp_incl_scan(c);
-    if (lane == 31) scan[w] = xs;
-    sel_sync();
-    int before = total + xs - c;
-    for (int i = 0; i < w; ++i) before += scan[i];
-    const int wtot = scan[0] + scan[1] + scan[2] + scan[3];
-    for (int r = 0; r < kBuildWin / kSelThreads; ++r) {
-      const int x = tid * (kBuildWin / kSelThreads) + r;
-      if (x < pw) {
-        uint32_t m[4];
-        page_masks(p0 + x, m);
-        if ((m[0] | m[1] | m[2] | m[3]) != 0u) {
-          const int lp = p0 + x;
-          const int ph = __ldg(pt_row + lp);
-          const bool ok = ph >= 0 && ph < p.num_pages;
-          if (!ok) set_status(A.status, SA_ERR_BAD_PAGE);
-          int4* dst = reinterpret_cast<int4*>(T + before);
-          dst[0] = make_int4(lp, ok ? ph : -1, 0, 0);
-          dst[1] = make_int4((int)m[0], (int)m[1], (int)m[2], (int)m[3]);
-          ++before;
-        }
-      }
-    }
-    total += wtot;
-    sel_sync();   // the window's bitmaps and scan words are reused
+    total += wpre[32];
+    sel_sync();   // the window's bitmaps and words are reused
   }
+  (void)lane;
   return total;
 }
 
@@ -430,8 +496,8 @@ __device__ int build_unit(const Params& p, const PArgs& A, const Smem& S, int u)
 
 // The last warp to park chunk k combines the kPC parked states (lane owns
 // dims [4 lane, 4 lane + 4)) into the chunk's partial, or into the output for
-// a unit held in one chunk; the last chunk of a unit merges the unit.  Then
-// the park buffer and the chunk's ring entry are released.
+// a unit held in one chunk, releases the park buffer and the chunk's ring
+// entry, and counts the chunk for the unit's merge (done by selector warps).
 __device__ __forceinline__ void combine_chunk(const Params& p, const PArgs& A, const Smem& S, int k, int lane,
                                            int* unit_done) {
   const int G = p.G;
@@ -474,18 +540,13 @@ __device__ __forceinline__ void combine_chunk(const Params& p, const PArgs& A, c
       }
     }
   }
-  if (nch > 1) {   // the last chunk of the unit merges the unit's partials
-    __threadfence();
-    __syncwarp();
-    int lastc = 0;
-    if (lane == 0) lastc = atomicAdd(unit_done + unit, 1) == nch - 1;
-    if (__shfl_sync(0xffffffffu, lastc, 0)) {
-      __threadfence();
-      merge_unit_warp(p, A, unit, pos0, nch, lane);
-    }
-  }
+  // the park buffer and the chunk's ring entry are free now (the fields above are in registers)
   __syncwarp();
-  if (lane == 0) st_release_block(&S.misc[M_COMB], k + 1);   // park buffer and ring entry free
+  if (lane == 0) st_release_block(&S.misc[M_COMB], k + 1);
+  if (nch > 1) {   // every lane's partial before lane 0's release of the count the merge waits for
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(unit_done + unit, 1);
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -518,6 +579,8 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
   int* unit_scored = gs + kGsHead;
   int* unit_heads = unit_scored + U;
   int* unit_done = unit_heads + U;
+  int* unit_pos0 = unit_done + U;
+  int* unit_nch1 = unit_pos0 + U;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kRows = item_rows(MODE);
@@ -587,8 +650,7 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
             S.misc[M_SEL_OK] = ok;
           }
           sel_sync();
-          if (!S.misc[M_SEL_OK]) break;
-          __threadfence();
+          if (!S.misc[M_SEL_OK]) break;   // (the merge loop below then times out too, bounded)
         }
         const float* sc = A.scores + ((size_t)b * p.Hq + h) * p.slots + j0;
         int* out_idx = A.sel_idx + ((size_t)b * p.Hq + h) * p.kcap;
@@ -597,12 +659,10 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
           group_topk<kSelThreads, 16, false, true>(sc, n, k, j0, out_idx, out_cnt, 1, *S.topk);
         else
           group_topk_stream<kSelThreads>(sc, n, k, j0, out_idx, out_cnt, 1, *S.topk);
-        __threadfence();
-        sel_sync();
-        if (tid == 0) S.misc[M_SEL_LAST] = atomicAdd(unit_heads + u, 1) == G - 1;
+        sel_sync();   // every thread's list entries before thread 0's release of the count
+        if (tid == 0) S.misc[M_SEL_LAST] = atom_acq_rel_gpu_add(unit_heads + u, 1) == G - 1;
         sel_sync();
         build = S.misc[M_SEL_LAST] != 0;
-        if (build) __threadfence();
       }
       if (!build) continue;
       // ---- the unit's tile list, its chunks, and (step) the tail summary
@@ -614,8 +674,7 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
       }
       const int C = max(A.C, (total + kPMaxChunksUnit - 1) / kPMaxChunksUnit);
       const int nch = (total + C - 1) / C;
-      __threadfence();   // the tiles before the queue entries that point at them
-      sel_sync();
+      sel_sync();   // every thread's tiles before the released queue flags below
       if (tid == 0) S.misc[M_QTAIL] = nch > 0 ? atomicAdd(&gs[kGsQTail], nch) : 0;
       sel_sync();
       const int pos0 = S.misc[M_QTAIL];
@@ -631,7 +690,6 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
         e->nch = nch;
         e->pos0 = pos0;
         e->kin = i;
-        __threadfence();
         st_release_gpu(&e->flag, 1);
       }
       if (A.summ_w != nullptr && warp == 0) {   // the block holding the newest token, re-summarised
@@ -640,9 +698,37 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
           summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, A.k_pool, A.page_table + (size_t)b * p.mpp,
                                A.summ_w, A.status);
       }
-      __threadfence();
       sel_sync();
-      if (tid == 0) atomicAdd(&gs[kGsUnitsBuilt], 1);
+      if (tid == 0) {
+        unit_pos0[u] = pos0;
+        st_release_gpu(unit_nch1 + u, nch + 1);
+        red_release_gpu_add(&gs[kGsUnitsBuilt], 1);
+      }
+    }
+    // ---- then merge tickets: a unit held in several chunks is merged once they are all combined
+    for (;;) {
+      if (tid == 0) S.misc[M_SEL_T] = atomicAdd(&gs[kGsMergeTicket], 1);
+      sel_sync();
+      const int u = S.misc[M_SEL_T];
+      sel_sync();
+      if (u >= U) break;
+      if (tid == 0) {
+        int nch1 = 0, ok = 1;
+        uint32_t i = 0;
+        while ((nch1 = ld_relaxed_gpu(unit_nch1 + u)) == 0 && ++i < kSpinGlobal) __nanosleep(64);
+        fence_acq_rel_gpu();
+        if (nch1 > 2) ok = wait_ge_gpu(unit_done + u, nch1 - 1);
+        if (i >= kSpinGlobal || !ok) {
+          set_status(A.status, SA_ERR_TIMEOUT);
+          nch1 = -1;   // stop: the waits of later tickets would run out too
+        }
+        S.misc[M_SEL_OK] = nch1;
+      }
+      sel_sync();
+      if (S.misc[M_SEL_OK] < 0) break;
+      const int nch = S.misc[M_SEL_OK] - 1;
+      if (nch > 1) merge_unit(p, A, u, __ldcg(unit_pos0 + u), nch);
+      sel_sync();
     }
   } else if (warp == kPCtl) {
     // ================================================================ control: chunk tickets -> ring
@@ -652,8 +738,9 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
       bool ok = true;
       if (lane == 0) {   // ring entry k % kPRing is free once chunk k - kPRing is combined
         uint32_t i = 0;
-        while (ld_acquire_block(&S.misc[M_COMB]) < k - kPRing + 1 && ++i < kSpin) __nanosleep(32);
+        while (ld_relaxed_block(&S.misc[M_COMB]) < k - kPRing + 1 && ++i < kSpin) __nanosleep(32);
         ok = i < kSpin;
+        fence_acq_rel_block();
       }
       ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
       const int t = __shfl_sync(0xffffffffu, tick, 0);
@@ -662,10 +749,17 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
       int state = ok ? 0 : 2;   // 0 wait, 1 entry, 2 end / timeout
       if (lane == 0 && ok) {
         for (uint32_t i = 0; i < kSpinGlobal; ++i) {
-          if (t < A.qcap && ld_acquire_gpu(&A.dq[t].flag) != 0) { state = 1; break; }
-          if (ld_acquire_gpu(&gs[kGsUnitsBuilt]) >= U && t >= ld_acquire_gpu(&gs[kGsQTail])) { state = 2; break; }
-          __nanosleep(64);
+          if (t < A.qcap && ld_relaxed_gpu(&A.dq[t].flag) != 0) { state = 1; break; }
+          if ((i & 7) == 7 && ld_relaxed_gpu(&gs[kGsUnitsBuilt]) >= U) {
+            fence_acq_rel_gpu();
+            if (t >= ld_relaxed_gpu(&gs[kGsQTail])) {
+              state = 2;
+              break;
+            }
+          }
+          __nanosleep(32);
         }
+        fence_acq_rel_gpu();
         if (state == 0) {
           set_status(A.status, SA_ERR_TIMEOUT);
           state = 2;
@@ -718,9 +812,17 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
     uint32_t phase = 0u;
     int src = (A.given || total_items == 0) ? 1 : 0;   // 0 score items, 1 decode chunks, 2 done
     bool failed = false;
-    int tick = 0;
-    if (src == 0 && lane == 0) tick = atomicAdd(&gs[kGsScoreTicket], 1);
+    // score items are claimed kItemBatch at a time (one atomic on one global
+    // counter per batch: per-item atomics on one address serialise); the next
+    // batch is claimed when the current one is half used
+    int tick = 0, tick_next = 0, tick_left = 0;
+    if (src == 0 && lane == 0) {
+      tick = atomicAdd(&gs[kGsScoreTicket], kItemBatch);
+      tick_next = atomicAdd(&gs[kGsScoreTicket], kItemBatch);
+    }
+    if (src == 0) tick_left = kItemBatch;
     int ck = 0, ci = 0;   // issue position: chunk ordinal, this warp's tile within it
+    int pub_seen = 0;     // chunks known to be published (read again only when the issue catches up)
 
     // Fill free slots (and queue park markers) ahead of the compute: score
     // items while the score ticket lasts, then this warp's tiles of the
@@ -731,7 +833,15 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
           if (busy == nslots) break;
           const int t = __shfl_sync(0xffffffffu, tick, 0);
           if (t >= total_items) { src = 1; continue; }
-          if (lane == 0) tick = atomicAdd(&gs[kGsScoreTicket], 1);   // the next ticket, in flight
+          if (--tick_left > 0) {
+            ++tick;
+          } else {   // the batch in hand is used up: move to the claimed one, claim another
+            tick_left = kItemBatch;
+            if (lane == 0) {
+              tick = tick_next;
+              tick_next = atomicAdd(&gs[kGsScoreTicket], kItemBatch);
+            }
+          }
           const int u = unit_of_item(S.items, U, t);
           const int b = u / p.Hk, kvh = u % p.Hk;
           const int L = min(__ldg(A.seq_lens + b), p.mpp * kP);
@@ -750,25 +860,29 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
           }
           ++n_iss; ++slot_ctr; ++busy;
         } else {
-          // lane 0 reads the published count (acquire) and the warp follows it
-          int pub = 0;
-          if (lane == 0) pub = ld_acquire_block(&S.misc[M_PUB]);
-          pub = __shfl_sync(0xffffffffu, pub, 0);
-          if (pub <= ck) {
-            if (n_iss > n_done) break;   // compute what is in flight first
-            int ok = 1;
-            if (lane == 0) {
-              uint32_t i = 0;
-              while (ld_acquire_block(&S.misc[M_PUB]) <= ck && ++i < kSpin) __nanosleep(32);
-              ok = i < kSpin;
+          // lane 0 reads the published count (relaxed; one acquire fence when it
+          // has moved) and the warp follows it
+          if (pub_seen <= ck) {
+            int pub = 0;
+            if (lane == 0) pub = ld_relaxed_block(&S.misc[M_PUB]);
+            pub = __shfl_sync(0xffffffffu, pub, 0);
+            if (pub <= ck) {
+              if (n_iss > n_done) break;   // compute what is in flight first
+              if (lane == 0) {
+                uint32_t i = 0;
+                while ((pub = ld_relaxed_block(&S.misc[M_PUB])) <= ck && ++i < kSpin) __nanosleep(32);
+              }
+              pub = __shfl_sync(0xffffffffu, pub, 0);
+              if (pub <= ck) {
+                if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
+                failed = true;
+                break;
+              }
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-              if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
-              failed = true;
-              break;
-            }
+            if (lane == 0) fence_acq_rel_block();
+            pub_seen = pub;
+            __syncwarp();   // the ring entries' contents, ordered after lane 0's acquire
           }
-          __syncwarp();   // the ring entry's contents, ordered after lane 0's acquire
           const RingHdr* h = S.hdr + ck % kPRing;
           const int unit = h->unit;
           if (unit < 0) { src = 2; break; }
@@ -820,9 +934,8 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
         break;
       }
       score_item<MODE>(p, A, my_slots + (size_t)e.y * kSlotB, e.z, e.w & 0xffff, e.w >> 16, lane);
-      __threadfence();   // the scores before the count that publishes them
-      __syncwarp();      // and every lane is done with the slot before it is refilled
-      if (lane == 0) atomicAdd(unit_scored + e.z, e.w >> 16);
+      __syncwarp();   // every lane's scores (and reads of the slot) before lane 0's release of the count
+      if (lane == 0) red_release_gpu_add(unit_scored + e.z, e.w >> 16);
       --busy;
     }
 
@@ -879,8 +992,9 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
         int ok = 1;
         if (lane == 0) {   // the park buffer is free once chunk k - 1 is combined
           uint32_t i = 0;
-          while (ld_acquire_block(&S.misc[M_COMB]) < k && ++i < kSpin) __nanosleep(32);
+          while (ld_relaxed_block(&S.misc[M_COMB]) < k && ++i < kSpin) __nanosleep(32);
           ok = i < kSpin;
+          fence_acq_rel_block();
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           if (lane == 0) set_status(A.status, SA_ERR_TIMEOUT);
@@ -933,18 +1047,14 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
   // ---- every role is done: the last CTA to leave zeroes the counters of this launch
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    S.misc[M_LASTCTA] = atomicAdd(&gs[kGsExit], 1) == (int)gridDim.x - 1;
-    if (S.misc[M_LASTCTA]) {
-      __threadfence();
-      S.misc[M_QTAIL] = min(ld_acquire_gpu(&gs[kGsQTail]), A.qcap);
-    }
+    S.misc[M_LASTCTA] = atom_acq_rel_gpu_add(&gs[kGsExit], 1) == (int)gridDim.x - 1;
+    if (S.misc[M_LASTCTA]) S.misc[M_QTAIL] = min(ld_relaxed_gpu(&gs[kGsQTail]), A.qcap);
   }
   __syncthreads();
   if (S.misc[M_LASTCTA]) {
     const int nq = S.misc[M_QTAIL];
     for (int i = tid; i < nq; i += blockDim.x) A.dq[i].flag = 0;
-    for (int i = tid; i < kGsHead + 3 * U; i += blockDim.x)
+    for (int i = tid; i < kGsHead + kGsPerUnit * U; i += blockDim.x)
       if (i != kGsExit) gs[i] = 0;
     __threadfence();
     __syncthreads();
@@ -959,7 +1069,7 @@ step_kernel(Params p, PArgs A, const __grid_constant__ CUtensorMap tmK, const __
 
 // ------------------------------------------------------------------ host
 
-int persist_chunk_tiles(const Params&) { return 16; }
+int persist_chunk_tiles(const Params&) { return kPMaxC; }
 
 size_t persist_qcap(const Params& p) {
   const int C = persist_chunk_tiles(p);
@@ -967,7 +1077,7 @@ size_t persist_qcap(const Params& p) {
   return (size_t)p.B * p.Hk * per_unit;
 }
 
-size_t persist_gs_bytes(const Params& p) { return ((size_t)kGsHead + 3 * (size_t)p.B * p.Hk) * sizeof(int); }
+size_t persist_gs_bytes(const Params& p) { return ((size_t)kGsHead + kGsPerUnit * (size_t)p.B * p.Hk) * sizeof(int); }
 
 size_t persist_partials_bytes(const Params& p) { return persist_qcap(p) * partial_stride(p.G) * sizeof(float); }
 

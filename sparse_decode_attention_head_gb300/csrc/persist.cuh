@@ -14,9 +14,12 @@ constexpr int kPMaxChunksUnit = 1024;   // chunks per (sequence, KV head) at mos
 constexpr int kPMaxUnits = 1024;        // (sequence, KV head) units per launch at most
 
 // Global hand-off state (ints in the workspace; zero between launches):
-// tickets and counts, then per unit: blocks scored, heads selected, chunks merged.
-constexpr int kGsScoreTicket = 0, kGsSelTicket = 1, kGsQTail = 2, kGsQHead = 3, kGsUnitsBuilt = 4, kGsExit = 5;
+// tickets and counts, then per unit: blocks scored, heads selected, chunks
+// combined, and its first queue position and chunk count + 1 (0: not built).
+constexpr int kGsScoreTicket = 0, kGsSelTicket = 1, kGsQTail = 2, kGsQHead = 3, kGsUnitsBuilt = 4, kGsExit = 5,
+              kGsMergeTicket = 6;
 constexpr int kGsHead = 8;
+constexpr int kGsPerUnit = 5;
 
 // One chunk of a unit's tile list in the global queue; `flag` is set last.
 struct PQEntry {
