@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["summarize.cu", "select.cu", "decode.cu", "merge.cu", "sa_api.cu", "noalloc.cu", "tables.cu", "step.cu",
-           "tokens.cu", "bypass.cu", "persist.cu"]
+           "tokens.cu", "bypass.cu"]
 
 
 def nvcc() -> str:

@@ -5,7 +5,6 @@
 
 #include <cuda.h>
 
-#include "persist.cuh"
 #include "sa_common.cuh"
 #include "sparsity.cuh"
 #include "tables.cuh"

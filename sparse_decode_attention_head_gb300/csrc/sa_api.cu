@@ -72,7 +72,7 @@ int make_params(const sa_problem* pr, Params* p) {
 }
 
 struct Layout {
-  size_t header, scores, tiles, ntiles, counters, partials, stage, pgs, pdq, ppart, total;
+  size_t header, scores, tiles, ntiles, counters, partials, stage, total;
 };
 
 Layout layout_of(const Params& p) {
@@ -92,12 +92,6 @@ Layout layout_of(const Params& p) {
   off = align_up(off + sa::decode_partials_bytes(p));
   l.stage = off;   // score-table candidates per chunk
   off = align_up(off + sa::tables_stage_bytes(p));
-  l.pgs = off;     // the persistent step's hand-off counters (zero between launches)
-  off = align_up(off + sa::persist_gs_bytes(p));
-  l.pdq = off;     // its chunk queue
-  off = align_up(off + sa::persist_qcap(p) * sizeof(sa::PQEntry));
-  l.ppart = off;   // its chunk partials
-  off = align_up(off + sa::persist_partials_bytes(p));
   l.total = off;
   return l;
 }
@@ -180,30 +174,6 @@ int num_sms_current() {
 
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-// Arguments of the persistent step over a workspace.
-sa::PArgs persist_args(const Layout& l, void* ws, const void* q, const void* summ_r, void* summ_w,
-                       const void* k_pool, const int32_t* page_table, const int32_t* seq_lens, const int32_t* sel_idx,
-                       const int32_t* sel_cnt, float* out, float* lse, int given) {
-  sa::PArgs A{};
-  A.q = static_cast<const __nv_bfloat16*>(q);
-  A.summ_r = static_cast<const __nv_bfloat16*>(summ_r);
-  A.summ_w = static_cast<__nv_bfloat16*>(summ_w);
-  A.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
-  A.page_table = page_table;
-  A.seq_lens = seq_lens;
-  A.sel_idx = const_cast<int*>(sel_idx);
-  A.sel_cnt = const_cast<int*>(sel_cnt);
-  A.scores = at<float>(ws, l.scores);
-  A.tiles = at<sa::Tile>(ws, l.tiles);
-  A.partials = at<float>(ws, l.ppart);
-  A.gs = at<int>(ws, l.pgs);
-  A.dq = at<sa::PQEntry>(ws, l.pdq);
-  A.out = out;
-  A.lse = lse;
-  A.status = at<int>(ws, l.header);
-  A.given = given;
-  return A;
-}
 
 }  // namespace sa_host
 
@@ -321,12 +291,6 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   if ((rc = make_kv_map(&tmV, v_pool, p)) != SA_OK) return rc;
   const Layout l = layout_of(p);
   cudaStream_t s = as_stream(stream);
-  if (sel_granularity == SA_SEL_BLOCK && logits_or_null == nullptr && sa::persist_supported(p, false)) {
-    // one persistent launch: tile lists, paged decode and merge as work queues
-    const sa::PArgs A = persist_args(l, ws, q, nullptr, nullptr, k_pool, page_table, seq_lens, sel_idx, sel_cnt, out,
-                                     lse, 1);
-    return sa::launch_persist(p, A, tmK, tmV, nsm, s);
-  }
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
                               at<int>(ws, l.ntiles), out, lse, at<int>(ws, l.header),
                               at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
@@ -380,12 +344,6 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
     E = sa::EstArgs{static_cast<const __nv_bfloat16*>(k_pool), page_table,
                     static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), kv_stats,
                     eps, rho, bypass, out, lse, status};
-  }
-  if (k_new == nullptr && kv_stats == nullptr && sa::persist_supported(p, true)) {
-    // the whole step in one persistent launch: scores, top-k, tiles, decode, merge, tail summary
-    const sa::PArgs A = persist_args(l, ws, q, summaries, summaries, k_pool, page_table, seq_lens, sel_idx, sel_cnt,
-                                     out, lse, 0);
-    return sa::launch_persist(p, A, tmK, tmV, nsm, s);
   }
   // the scores never read the newest token's block (it is in the window), so
   // the append and the tail summary can follow them

@@ -137,52 +137,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// GPU-scope acquire load / release store (cross-CTA hand-offs through global memory)
-__device__ __forceinline__ int ld_acquire_gpu(const int* x) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(int* x, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
-}
-// Relaxed GPU-scope load (coherent at L2, no L1 invalidation): for spinning
-// on a flag; the acquire is one fence_acq_rel_gpu() once the flag is seen.
-__device__ __forceinline__ int ld_relaxed_gpu(const int* x) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-// Release reduction / acquire-release atomic add at GPU scope.  A release is
-// cumulative: writes of other threads ordered before it by a barrier
-// (__syncwarp, bar.sync) are published with it.
-__device__ __forceinline__ void red_release_gpu_add(int* x, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
-}
-__device__ __forceinline__ int atom_acq_rel_gpu_add(int* x, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(x), "r"(v) : "memory");
-  return old;
-}
-// Relaxed CTA-scope load and acquire-release fence: spin on a shared counter
-// with the load, fence once when the awaited value is seen.
-__device__ __forceinline__ int ld_relaxed_block(const int* x) {
-  int v;
-  asm volatile("ld.relaxed.cta.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_acq_rel_block() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
-// CTA-scope acquire load / release store (hand-offs between warps through shared memory)
-__device__ __forceinline__ int ld_acquire_block(const int* x) {
-  int v;
-  asm volatile("ld.acquire.cta.b32 %0, [%1];" : "=r"(v) : "l"(x) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_block(int* x, int v) {
-  asm volatile("st.release.cta.b32 [%0], %1;" ::"l"(x), "r"(v) : "memory");
-}
-
 // ---------------------------------------------------------------- mbarrier / TMA
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

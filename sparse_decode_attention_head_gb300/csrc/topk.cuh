@@ -63,9 +63,8 @@ __device__ __forceinline__ int group_excl_scan(int v, int* tmp, int bar_id) {
 // of sc[r * row_stride + i] over nrows rows (a selection shared by a KV
 // head's query heads) -- a separate instantiation, so that the one-row case
 // keeps its loads independent of each other.  k_req: blocks to keep.  Writes
-// out[0..) and *cnt_out.  CG: the scores are read from L2 only (written by
-// other CTAs of the same launch).
-template <int GROUP, int KPT, bool ROWS = false, bool CG = false>
+// out[0..) and *cnt_out.
+template <int GROUP, int KPT, bool ROWS = false>
 __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int base_idx, int* __restrict__ out,
                            int* __restrict__ cnt_out, int bar_id, TopkScratch& S, int nrows = 1,
                            size_t row_stride = 0) {
@@ -84,9 +83,9 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
     const int i = tg * KPT + q;
     float x = 0.f;
     if (i < n) {
-      x = CG ? __ldcg(sc + i) : sc[i];
+      x = sc[i];
       if (ROWS)
-        for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, CG ? __ldcg(sc + r * row_stride + i) : sc[r * row_stride + i]);
+        for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, sc[r * row_stride + i]);
     }
     key[q] = i < n ? order_key(x) : 0u;
     if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
@@ -191,127 +190,6 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
       if (key[q] == T) { t = r < need_eq; ++r; }
       if (t) out[pos++] = base_idx + i;
     }
-  }
-  if (tg == 0) *cnt_out = k;
-}
-
-// Group-collective top-k with the same result as group_topk for any n, that
-// holds no keys in registers: every pass re-reads the scores from L2 (they
-// were written by other CTAs of the same launch).  The radix passes read the
-// scores strided over the group (coalesced); the final compaction gives each
-// thread a contiguous index range, so the kept blocks come out ascending.
-template <int GROUP>
-__device__ void group_topk_stream(const float* __restrict__ sc, int n, int k_req, int base_idx, int* __restrict__ out,
-                                  int* __restrict__ cnt_out, int bar_id, TopkScratch& S) {
-  const int tg = threadIdx.x % GROUP, lane = tg & 31, w = tg >> 5;
-  const int k = min(k_req, n);
-  if (k >= n || k <= 0) {
-    const int m = k >= n ? n : 0;
-    for (int i = tg; i < m; i += GROUP) out[i] = base_idx + i;
-    if (tg == 0) *cnt_out = m;
-    return;
-  }
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int i = tg; i < n; i += GROUP) {
-    const uint32_t key = order_key(__ldcg(sc + i));
-    kmin = min(kmin, key);
-    kmax = max(kmax, key);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) { S.red[0][w] = (int)kmin; S.red[1][w] = (int)kmax; }
-  group_sync(bar_id, GROUP);
-  uint32_t gmin = 0xffffffffu, gmax = 0u;
-  for (int i = 0; i < GROUP / 32; ++i) { gmin = min(gmin, (uint32_t)S.red[0][i]); gmax = max(gmax, (uint32_t)S.red[1][i]); }
-  group_sync(bar_id, GROUP);
-  const int common = gmin == gmax ? 32 : __clz(gmin ^ gmax);
-  uint32_t mask = common >= 32 ? 0xffffffffu : (common == 0 ? 0u : (0xffffffffu << (32 - common)));
-  uint32_t prefix = gmin & mask;
-  int krem = k;
-  for (int top = 32 - common; top > 0; top -= 8) {
-    const int shift = max(0, top - 8);
-    const uint32_t dmask = (1u << (top - shift)) - 1u;
-    for (int i = tg; i < 256; i += GROUP) S.hist[i] = 0;
-    group_sync(bar_id, GROUP);
-    for (int i = tg; i < n; i += GROUP) {
-      const uint32_t key = order_key(__ldcg(sc + i));
-      if ((key & mask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1);
-    }
-    group_sync(bar_id, GROUP);
-    if (w == 0) {
-      int cnt[8], tot = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { cnt[q] = S.hist[255 - 8 * lane - q]; tot += cnt[q]; }
-      const int incl = warp_incl_scan(tot);
-      int above = incl - tot;
-      if (above < krem && krem <= incl) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (above < krem && krem <= above + cnt[q]) {
-            S.prefix = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
-            S.krem = krem - above;
-            S.bcnt = cnt[q];
-          }
-          above += cnt[q];
-        }
-      }
-    }
-    if (tg == 0) S.nc = 0;
-    group_sync(bar_id, GROUP);
-    prefix = S.prefix;
-    krem = S.krem;
-    mask |= dmask << shift;
-    if (shift > 0 && S.bcnt <= 32) {
-      for (int i = tg; i < n; i += GROUP) {
-        const uint32_t key = order_key(__ldcg(sc + i));
-        if ((key & mask) == prefix) S.cand[atomicAdd(&S.nc, 1)] = key;
-      }
-      group_sync(bar_id, GROUP);
-      if (w == 0) {
-        const int nc = S.nc;
-        const uint32_t mine = lane < nc ? S.cand[lane] : 0u;
-        int gt_cnt = 0, ge_cnt = 0;
-        for (int j = 0; j < nc; ++j) {
-          const uint32_t o = __shfl_sync(0xffffffffu, mine, j);
-          gt_cnt += o > mine;
-          ge_cnt += o >= mine;
-        }
-        if (lane < nc && gt_cnt < krem && krem <= ge_cnt) {
-          S.prefix = mine;
-          S.krem = krem - gt_cnt;
-        }
-      }
-      group_sync(bar_id, GROUP);
-      prefix = S.prefix;
-      krem = S.krem;
-      mask = 0xffffffffu;
-      group_sync(bar_id, GROUP);
-      break;
-    }
-    group_sync(bar_id, GROUP);
-  }
-  const uint32_t T = prefix;
-  const int need_eq = krem;
-  const int per = (n + GROUP - 1) / GROUP;
-  const int a = min(n, tg * per), e = min(n, a + per);
-  int eq = 0, gt = 0;
-  for (int i = a; i < e; ++i) {
-    const uint32_t key = order_key(__ldcg(sc + i));
-    eq += key == T;
-    gt += key > T;
-  }
-  const int eq_before = group_excl_scan<GROUP>(eq, S.red[0], bar_id);
-  const int take = gt + max(0, min(eq, need_eq - eq_before));
-  int pos = group_excl_scan<GROUP>(take, S.red[1], bar_id);
-  int r = eq_before;
-  for (int i = a; i < e; ++i) {
-    const uint32_t key = order_key(__ldcg(sc + i));
-    bool t = key > T;
-    if (key == T) { t = r < need_eq; ++r; }
-    if (t) out[pos++] = base_idx + i;
   }
   if (tg == 0) *cnt_out = k;
 }
