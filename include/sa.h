@@ -236,6 +236,28 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool,
                    int32_t* sel_cnt, float* out, float* lse, void* ws,
                    void* stream);
 
+/* A prepared decode step: sa_decode_step on fixed buffers, captured once into
+ * a CUDA graph inside the library and replayed by one call.  For a serving
+ * loop that reuses its buffers (fresh contents each step, same addresses):
+ * the launch costs one graph launch on the host instead of the step's
+ * argument checks, descriptor set-up and four kernel launches.
+ *   sa_step_plan_create: checks the arguments as sa_decode_step does (the
+ *     same errors, returned before anything is captured), then captures the
+ *     step's launches on a private stream and instantiates the graph.  Not
+ *     inside a stream capture.  Allocates host and graph resources.
+ *   sa_step_plan_launch: one sa_decode_step on the plan's buffers, async on
+ *     `stream`; the buffers' current contents are used.  Calls that share the
+ *     plan's workspace must be ordered on one stream.
+ *   sa_step_plan_destroy: frees the plan (NULL is a no-op); the caller keeps
+ *     the buffers. */
+typedef struct sa_step_plan sa_step_plan;
+
+int sa_step_plan_create(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* page_table, const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
+                        int32_t* sel_cnt, float* out, float* lse, void* ws, sa_step_plan** plan);
+int sa_step_plan_launch(sa_step_plan* plan, void* stream);
+int sa_step_plan_destroy(sa_step_plan* plan);
+
 /* The new token's key and value rows into the pools: for every (b, kv head)
  * with L = seq_lens[b] > 0 (L counts the new token), k_new[b][kvh][:] and
  * v_new[b][kvh][:] (bf16 [B][Hk][D], 16-byte aligned) are written at

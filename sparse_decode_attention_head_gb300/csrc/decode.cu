@@ -11,10 +11,11 @@
 // merged with the same identity, in chunk order, stabilised by the running
 // maximum (the review's comment on Sec. 3.3).
 //
-// Kernel 1 (tile builder, one CTA per (sequence, KV head)): the union over
-// the G query heads of the pages to read, as an ascending list of tiles; a
-// tile is one 16-token page with a G-bit head mask per token, so the rows a
-// GQA group shares are read once (SPIN abstract / Fig. 6: paged KV substrate).
+// Kernel 1 (tile builder, one CTA per (sequence, KV head, window of 4096
+// pages)): the union over the G query heads of the pages to read, as an
+// ascending list of tiles per window; a tile is one 16-token page with a
+// G-bit head mask per token, so the rows a GQA group shares are read once
+// (SPIN abstract / Fig. 6: paged KV substrate).
 //
 // Kernel 2 (decode, persistent, dynamically scheduled): the tile lists are cut
 // into chunks of C tiles that never cross a unit; CTA c starts on chunk c and
@@ -61,11 +62,10 @@ constexpr int kBuildThreads = 1024;
 __global__ void __launch_bounds__(kBuildThreads)
 build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                    const int* __restrict__ sel_idx, const int* __restrict__ sel_cnt, int gran,
-                   Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
-                   float* __restrict__ lse, int* status, int* ticket) {
+                   Tile* __restrict__ tiles, int* __restrict__ ntiles, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
   extern __shared__ int smem_b[];   // build_smem_bytes(mpp): window flags, then window masks
   __shared__ int scan_tmp[32];
   const int win = min(p.mpp, kWinPages);
@@ -73,8 +73,8 @@ build_tiles_kernel(Params p, const int* __restrict__ seq_lens, const int* __rest
   const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
   const uint32_t active = unit_active_heads(p, b, kvh);
   build_unit_tiles<kBuildThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0, gran, tiles,
-                                  ntiles, out, lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win),
-                                  scan_tmp, active);
+                                  ntiles, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win),
+                                  scan_tmp, active, blockIdx.z, 1);
 }
 
 // ------------------------------------------------------------------ decode
@@ -86,6 +86,7 @@ struct DecodeArgs {
   const int* ntiles;
   float* partials;   // [chunks][partial_stride(G)]: per chunk O[G][kD], max[G], sum[G]
   int* chunk_prefix; // [U + 1]: chunks before unit u (written by CTA 0 for the merge kernel)
+  int nwin;          // tile-list segments (windows) per unit
   int* ticket;       // chunk ticket counter (zeroed by the tile builder)
   float* out;
   float* lse;
@@ -150,6 +151,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int G = p.G;
   const int U = p.B * p.Hk;
+  const int NW = A.nwin;
+  const int SG = U * NW;   // tile-list segments: unit u, window w is segment u * NW + w
   // nslots page slots (a multiple of kConsWarps), then small state
   uint8_t* s_tiles = smem;                                                   // nslots * kTileBytes
   uint8_t* s_p = s_tiles + (size_t)nslots * kTileBytes;                      // kConsWarps * 512
@@ -160,9 +163,9 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_assign + kChunkRing * kConsWarps);   // nslots
   uint64_t* s_empty = s_full + nslots;                                       // nslots
   int* s_misc = reinterpret_cast<int*>(s_empty + nslots);                    // 32 ints
-  int* s_prefix = s_misc + 32;                                               // U + 1: tiles before unit u
-  int* s_cprefix = s_prefix + U + 1;                                         // U + 1: chunks before unit u
-  uint8_t* s_umask = reinterpret_cast<uint8_t*>(s_cprefix + U + 1);         // U bytes: heads left out (bypass)
+  int* s_prefix = s_misc + 32;                                               // SG + 1: tiles before segment s
+  int* s_cprefix = s_prefix + SG + 1;                                        // SG + 1: chunks before segment s
+  uint8_t* s_umask = reinterpret_cast<uint8_t*>(s_cprefix + SG + 1);        // U bytes: heads left out (bypass)
   // s_misc: [17] chunks published, [18] chunks combined, [19] chunks fully
   // issued, [20] consumer warps parked on the current chunk
 
@@ -179,20 +182,19 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     s_misc[19] = 0;
     s_misc[20] = 0;
   }
-  // prefix over the units' tile counts (block-wide scan); the chunk size
+  if (p.bypass != nullptr)   // heads answered by the sparsity bypass: their rows are not written
+    for (int i = tid; i < U; i += blockDim.x) {
+      int m = 0;
+      for (int g = 0; g < G; ++g) m |= (p.bypass[(size_t)i * G + g] != 0 ? 1 : 0) << g;
+      s_umask[i] = (uint8_t)m;
+    }
+  // prefix over the segments' tile counts (block-wide scan); the chunk size
   // follows from the total so that every CTA derives the same chunk list
-  const int per = (U + blockDim.x - 1) / blockDim.x;
-  const int a = min(U, tid * per), e = min(U, a + per);
+  const int per = (SG + blockDim.x - 1) / blockDim.x;
+  const int a = min(SG, tid * per), e = min(SG, a + per);
   {
     int cnt = 0;
-    for (int i = a; i < e; ++i) {
-      cnt += A.ntiles[i];
-      if (p.bypass != nullptr) {   // heads answered by the sparsity bypass: their rows are not written
-        int m = 0;
-        for (int g = 0; g < G; ++g) m |= (p.bypass[(size_t)i * G + g] != 0 ? 1 : 0) << g;
-        s_umask[i] = (uint8_t)m;
-      }
-    }
+    for (int i = a; i < e; ++i) cnt += A.ntiles[i];
     int x = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -207,10 +209,10 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       s_prefix[i] = before;
       before += A.ntiles[i];
     }
-    if (tid == blockDim.x - 1) s_prefix[U] = before;
+    if (tid == blockDim.x - 1) s_prefix[SG] = before;
   }
   __syncthreads();
-  const int T = s_prefix[U];
+  const int T = s_prefix[SG];
   const int C = max(kMinChunk, (T + kChunksPerCta * (int)gridDim.x - 1) / (kChunksPerCta * (int)gridDim.x));
   {
     int cnt = 0;
@@ -229,13 +231,13 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       s_cprefix[i] = before;
       before += (s_prefix[i + 1] - s_prefix[i] + C - 1) / C;
     }
-    if (tid == blockDim.x - 1) s_cprefix[U] = before;
+    if (tid == blockDim.x - 1) s_cprefix[SG] = before;
   }
   __syncthreads();
-  const int NCH = s_cprefix[U];
+  const int NCH = s_cprefix[SG];
   const int PS = partial_stride(G);
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= U; i += blockDim.x) A.chunk_prefix[i] = s_cprefix[i];
+  if (blockIdx.x == 0)   // chunks before unit u, for the merge kernel
+    for (int i = tid; i <= U; i += blockDim.x) A.chunk_prefix[i] = s_cprefix[i * NW];
 
   // ------------------------------------------------------------ producer warp
   // Takes chunks from the global ticket counter (one taken ahead) and
@@ -255,12 +257,14 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
       c.kin = c.nch = c.t0 = c.nt = 0;
       c.pad[0] = c.pad[1] = c.pad[2] = 0;
       if (t < NCH) {
-        const int u = unit_of(s_cprefix, U, t);
+        const int sg = unit_of(s_cprefix, SG, t);   // segment holding chunk t
+        const int u = sg / NW;
+        const int kseg = t - s_cprefix[sg];          // chunk within the segment
         c.unit = u;
-        c.kin = t - s_cprefix[u];
-        c.nch = s_cprefix[u + 1] - s_cprefix[u];
-        c.t0 = c.kin * C;
-        c.nt = min(C, s_prefix[u + 1] - s_prefix[u] - c.t0);
+        c.kin = t - s_cprefix[u * NW];
+        c.nch = s_cprefix[(u + 1) * NW] - s_cprefix[u * NW];
+        c.t0 = (sg - u * NW) * kWinPages + kseg * C;   // entry within the unit's tile array
+        c.nt = min(C, s_prefix[sg + 1] - s_prefix[sg] - kseg * C);
       }
       return c;
     };
@@ -603,7 +607,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     // ---- the last warp combines the kConsWarps states: lane owns dims [4 lane, 4 lane + 4)
     if (lane == 0) s_misc[20] = 0;
     const bool whole = ci.nch == 1;
-    float* part = A.partials + (size_t)(s_cprefix[u] + ci.kin) * PS;
+    float* part = A.partials + (size_t)(s_cprefix[u * NW] + ci.kin) * PS;
     for (int g = 0; g < G; ++g) {
       float M = -INFINITY;
 #pragma unroll
@@ -663,7 +667,7 @@ merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __r
   pdl_trigger();
   const int g = blockIdx.x, u = blockIdx.y;
   const int c0 = chunk_prefix[u], nch = chunk_prefix[u + 1] - c0;
-  if (nch <= 1) return;
+  if (nch == 1) return;   // written by the decode; no chunk (nothing attended): O = 0, lse = -inf below
   const int G = p.G, PS = partial_stride(G);
   const int tid = threadIdx.x;
   const float* P = partials + (size_t)c0 * PS;
@@ -705,44 +709,52 @@ merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __r
   if (tid == 0) lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
 }
 
-size_t decode_smem_bytes_n(int U, int G, int nslots) {
+// SG: tile-list segments (units x windows); the bypass mask takes SG >= U bytes.
+size_t decode_smem_bytes_n(int SG, int G, int nslots) {
   return 1024 + (size_t)nslots * kTileBytes + kConsWarps * 512 + (size_t)kConsWarps * G * kPart * 4 +
          nslots * sizeof(SlotInfo) + kChunkRing * sizeof(ChunkInfo) + kChunkRing * kConsWarps * 4 +
          2 * nslots * 8 + 32 * 4 +
-         (2 * (size_t)(U + 1) + (U + 3) / 4) * 4;
+         (2 * (size_t)(SG + 1) + (SG + 3) / 4) * 4;
 }
 
 // Slot count: the largest multiple of kConsWarps (<= 16) that still lets two
 // CTAs share an SM; at least kConsWarps.
-int decode_slots(int U, int G) {
+int decode_slots(int SG, int G) {
   const size_t per_sm = 228 * 1024, reserve = 1024;
   int best = kConsWarps;
   for (int n = kConsWarps; n <= 16; n += kConsWarps)
-    if (2 * (decode_smem_bytes_n(U, G, n) + reserve) <= per_sm) best = n;
+    if (2 * (decode_smem_bytes_n(SG, G, n) + reserve) <= per_sm) best = n;
   return best;
 }
 
-size_t decode_smem_bytes(int U) { return decode_smem_bytes_n(U, kMaxG, kConsWarps); }
-
-// Chunks never exceed kChunksPerCta * grid + U (the chunk size grows with the
-// total beyond kMinChunk tiles per chunk), and the grid never exceeds kMaxCtas.
-size_t decode_partials_bytes(const Params& p) {
-  return ((size_t)kChunksPerCta * kMaxCtas + (size_t)p.B * p.Hk) * partial_stride(p.G) * sizeof(float);
+// smallest shared-memory request of the decode for the problem (its fewest slots)
+size_t decode_smem_bytes(const Params& p) {
+  return decode_smem_bytes_n(p.B * p.Hk * num_windows(p.mpp), kMaxG, kConsWarps);
 }
+
+// Chunks never exceed kChunksPerCta * grid + (segments) (the chunk size grows
+// with the total beyond kMinChunk tiles per chunk), and the grid never
+// exceeds kMaxCtas.
+size_t decode_partials_bytes(const Params& p) {
+  return ((size_t)kChunksPerCta * kMaxCtas + (size_t)p.B * p.Hk * num_windows(p.mpp)) * partial_stride(p.G) *
+         sizeof(float);
+}
+
+size_t ntiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * num_windows(p.mpp) * sizeof(int); }
 
 size_t tiles_bytes(const Params& p) { return (size_t)p.B * p.Hk * p.mpp * sizeof(Tile); }
 
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
-                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       int* ticket, cudaStream_t stream) {
+                       const int* sel_cnt, int gran, void* tiles, int* ntiles, int* status, int* ticket,
+                       cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
   // static + dynamic shared memory can pass the 48 KB default even when the
   // dynamic part alone does not: always opt in (cached per kernel)
   smem_limit_at_least(reinterpret_cast<const void*>(build_tiles_kernel), (int)smem);
-  dim3 grid(p.Hk, p.B);
+  dim3 grid(p.Hk, p.B, num_windows(p.mpp));   // one CTA per window of each unit
   const cudaError_t e = launch_pdl(build_tiles_kernel, grid, dim3(kBuildThreads), smem, stream, p, seq_lens,
-                                   page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, out, lse,
-                                   status, ticket);
+                                   page_table, sel_idx, sel_cnt, gran, static_cast<Tile*>(tiles), ntiles, status,
+                                   ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -750,8 +762,9 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
   const int U = p.B * p.Hk;
-  const int nslots = decode_slots(U, p.G);
-  const size_t smem = decode_smem_bytes_n(U, p.G, nslots);
+  const int SG = U * num_windows(p.mpp);
+  const int nslots = decode_slots(SG, p.G);
+  const size_t smem = decode_smem_bytes_n(SG, p.G, nslots);
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
   void (*kern)(Params, DecodeArgs, const CUtensorMap, const CUtensorMap, int) =
       logits != nullptr ? decode_kernel<true> : decode_kernel<false>;
@@ -765,6 +778,7 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.ntiles = ntiles;
   A.partials = partials;
   A.chunk_prefix = counters;
+  A.nwin = num_windows(p.mpp);
   A.ticket = counters + U + 1;
   A.out = out;
   A.lse = lse;

@@ -19,20 +19,20 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
                 cudaStream_t stream);
 size_t topk_smem_bytes(const Params& p);
 int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_table, const int* sel_idx,
-                       const int* sel_cnt, int gran, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                       int* ticket, cudaStream_t stream);
+                       const int* sel_cnt, int gran, void* tiles, int* ntiles, int* status, int* ticket,
+                       cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
                   float* partials, int* counters, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
-size_t decode_smem_bytes(int U);
+size_t decode_smem_bytes(const Params& p);
 size_t decode_partials_bytes(const Params& p);
 size_t tiles_bytes(const Params& p);
+size_t ntiles_bytes(const Params& p);
 int launch_lse_merge(int n_rows, int D, const float* o_a, const float* lse_a, const float* o_b,
                      const float* lse_b, float* o, float* lse, cudaStream_t stream);
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
                       const void* k_new, const void* v_new, float* stats, void* summ, const int* sel_idx, int* sel_cnt,
-                      void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
-                      cudaStream_t stream);
+                      void* tiles, int* ntiles, int* status, int* ticket, cudaStream_t stream);
 int launch_append_kv(const Params& p, const int* seq_lens, const int* page_table, const void* k_new, const void* v_new,
                      void* k_pool, void* v_pool, int* status, cudaStream_t stream);
 int launch_token_topk(const Params& p, const void* q, const void* k_pool, const int* page_table, const int* seq_lens,
@@ -40,8 +40,8 @@ int launch_token_topk(const Params& p, const void* q, const void* k_pool, const 
                       int* status, cudaStream_t stream);
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
                         void* k_pool, void* v_pool, const void* k_new, const void* v_new, float* stats, void* summ,
-                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                        int* ticket, cudaStream_t stream);
+                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, int* status, int* ticket,
+                        cudaStream_t stream);
 int launch_kv_stats(const Params& p, const void* k_pool, const void* v_pool, const int* page_table,
                     const int* seq_lens, float* stats, int* status, cudaStream_t stream);
 int launch_sparsity(const Params& p, const void* q, const int* seq_lens, const EstArgs& E, cudaStream_t stream);

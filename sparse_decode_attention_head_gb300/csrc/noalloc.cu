@@ -85,8 +85,8 @@ NoAllocLayout layout_of(const sa::Params& p) {
   off = up256(off + sizeof(int));
   l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
   off = up256(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
-  l.ntiles = off;
-  off = up256(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.ntiles = off;   // tile counts per (unit, window)
+  off = up256(off + sa::ntiles_bytes(p));
   l.tiles = off;
   off = up256(off + sa::tiles_bytes(p));
   l.partials = off;
@@ -132,7 +132,7 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   if (sel_granularity != SA_SEL_BLOCK && sel_granularity != SA_SEL_TOKEN) return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
-  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const NoAllocLayout l = layout_of(p);
   if (l.total > kNoAllocScratchBytes) return SA_ERR_CAPACITY;   // problem too large for the fixed scratch
   void* base = nullptr;
@@ -151,7 +151,7 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   // chunk ticket; the decode writes the chunk prefix before the merge reads it)
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
-                              reinterpret_cast<int*>(b + l.ntiles), out, lse, status, counters + p.B * p.Hk + 1, s);
+                              reinterpret_cast<int*>(b + l.ntiles), status, counters + p.B * p.Hk + 1, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
                            reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,

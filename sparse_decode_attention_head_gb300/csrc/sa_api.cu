@@ -84,8 +84,8 @@ Layout layout_of(const Params& p) {
   off = align_up(off + (size_t)p.B * p.Hq * p.slots * sizeof(float));
   l.tiles = off;
   off = align_up(off + sa::tiles_bytes(p));
-  l.ntiles = off;
-  off = align_up(off + (size_t)p.B * p.Hk * sizeof(int));
+  l.ntiles = off;   // tile counts per (unit, window)
+  off = align_up(off + sa::ntiles_bytes(p));
   l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
   off = align_up(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
   l.partials = off;
@@ -283,7 +283,7 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(ws))
     return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
-  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const int nsm = num_sms_current();
   if (nsm <= 0) return SA_ERR_CUDA;
   CUtensorMap tmK, tmV;
@@ -292,7 +292,7 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   const Layout l = layout_of(p);
   cudaStream_t s = as_stream(stream);
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
-                              at<int>(ws, l.ntiles), out, lse, at<int>(ws, l.header),
+                              at<int>(ws, l.ntiles), at<int>(ws, l.header),
                               at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
@@ -324,7 +324,7 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   if ((k_new == nullptr) != (v_new == nullptr)) return SA_ERR_INVALID_ARG;
   if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return SA_ERR_INVALID_ARG;
   if ((size_t)p.mpp * sizeof(int) > 200 * 1024) return SA_ERR_UNSUPPORTED;
-  if (sa::decode_smem_bytes(p.B * p.Hk) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  if (sa::decode_smem_bytes(p) > 227 * 1024) return SA_ERR_UNSUPPORTED;
   const int nsm = num_sms_current();
   if (nsm <= 0) return SA_ERR_CUDA;
   CUtensorMap tmK, tmV;
@@ -352,11 +352,11 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   if (kv_stats != nullptr) p.bypass = bypass;
   int* ticket = at<int>(ws, l.counters) + p.B * p.Hk + 1;
   rc = sa::launch_select_build(p, scores, seq_lens, page_table, kp, vp, k_new, v_new, kv_stats, summaries, sel_idx,
-                               sel_cnt, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+                               sel_cnt, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), status, ticket, s);
   if (rc == SA_ERR_UNSUPPORTED) {   // candidates beyond the fused kernel's capacity: two kernels
     if ((rc = sa::launch_topk(p, scores, seq_lens, sel_idx, sel_cnt, s)) != SA_OK) return rc;
     rc = sa::launch_build_step(p, seq_lens, page_table, kp, vp, k_new, v_new, kv_stats, summaries, sel_idx, sel_cnt,
-                               at<void>(ws, l.tiles), at<int>(ws, l.ntiles), out, lse, status, ticket, s);
+                               at<void>(ws, l.tiles), at<int>(ws, l.ntiles), status, ticket, s);
   }
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
@@ -372,6 +372,63 @@ int sa_decode_step(const sa_problem* prob, const void* q, const void* k_pool, co
                    int32_t* sel_cnt, float* out, float* lse, void* ws, void* stream) {
   return decode_step_impl(prob, q, nullptr, nullptr, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx,
                           sel_cnt, out, lse, ws, stream);
+}
+
+struct sa_step_plan {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+int sa_step_plan_create(const sa_problem* prob, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* page_table, const int32_t* seq_lens, void* summaries, int32_t* sel_idx,
+                        int32_t* sel_cnt, float* out, float* lse, void* ws, sa_step_plan** plan) {
+  if (plan == nullptr) return SA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  // the host-visible checks first, so that a bad argument returns before any capture
+  Params p;
+  int rc = make_params(prob, &p);
+  if (rc != SA_OK) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !summaries || !sel_idx || !sel_cnt || !out || !lse ||
+      !ws)
+    return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summaries) || !aligned16(out) ||
+      !aligned16(ws))
+    return SA_ERR_INVALID_ARG;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return SA_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return SA_ERR_CUDA;
+  }
+  rc = decode_step_impl(prob, q, nullptr, nullptr, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt,
+                        out, lse, ws, cs);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (rc != SA_OK || ec != cudaSuccess) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    return rc != SA_OK ? rc : SA_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return SA_ERR_CUDA;
+  }
+  *plan = new sa_step_plan{g, ex};
+  return SA_OK;
+}
+
+int sa_step_plan_launch(sa_step_plan* plan, void* stream) {
+  if (plan == nullptr) return SA_ERR_INVALID_ARG;
+  return cudaGraphLaunch(plan->exec, as_stream(stream)) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+int sa_step_plan_destroy(sa_step_plan* plan) {
+  if (plan == nullptr) return SA_OK;
+  cudaGraphExecDestroy(plan->exec);
+  cudaGraphDestroy(plan->graph);
+  delete plan;
+  return SA_OK;
 }
 
 int sa_decode_step_append(const sa_problem* prob, const void* q, const void* k_new, const void* v_new, void* k_pool,

@@ -18,9 +18,9 @@
 
 namespace sa {
 
-// Tile list of one (sequence, KV head) by warps 0..30, and the incremental
-// summary of its block holding token L - 1 by warp 31, which takes no part
-// in the builder's barriers.
+// Tile list of one window of one (sequence, KV head) by warps 0..30, and (in
+// the window-0 CTA) the incremental summary of its block holding token L - 1
+// by warp 31, which takes no part in the builder's barriers.
 constexpr int kStepBuildThreads = 1024;
 constexpr int kStepTileThreads = kStepBuildThreads - 32;
 
@@ -28,15 +28,16 @@ __global__ void __launch_bounds__(kStepBuildThreads)
 build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restrict__ page_table,
                   __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const __nv_bfloat16* __restrict__ k_new,
                   const __nv_bfloat16* __restrict__ v_new, float* stats, __nv_bfloat16* __restrict__ summ,
-                  const int* sel_idx, int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles,
-                  float* __restrict__ out, float* __restrict__ lse, int* status, int* ticket) {
+                  const int* sel_idx, int* sel_cnt, Tile* __restrict__ tiles, int* __restrict__ ntiles, int* status,
+                  int* ticket) {
   pdl_wait();
   pdl_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
   extern __shared__ int smem_b[];   // build_smem_bytes(mpp): window flags, then window masks
   __shared__ int scan_tmp[32];
   const int kvh = blockIdx.x, b = blockIdx.y;
   if (threadIdx.x >= kStepTileThreads) {
+    if (blockIdx.z != 0) return;
     const int L = min(seq_lens[b], p.mpp * kP);
     if (k_new != nullptr) {
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
@@ -50,26 +51,27 @@ build_step_kernel(Params p, const int* __restrict__ seq_lens, const int* __restr
   const size_t h0 = (size_t)b * p.Hq + kvh * p.G;
   const uint32_t active = unit_active_heads(p, b, kvh);
   build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, sel_idx + h0 * p.kcap, sel_cnt + h0,
-                                     SA_SEL_BLOCK, tiles, ntiles, out, lse, status, smem_b,
-                                     reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active);
-  // the builder's reads of the counts ended at its last barrier: heads
-  // answered by the sparsity bypass report no selection
-  if (p.bypass != nullptr && threadIdx.x < p.G && p.bypass[h0 + threadIdx.x]) sel_cnt[h0 + threadIdx.x] = 0;
+                                     SA_SEL_BLOCK, tiles, ntiles, status, smem_b,
+                                     reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active, blockIdx.z, 1);
+  // heads answered by the sparsity bypass report no selection (the builders
+  // of every window leave those heads out whatever their counts read)
+  if (blockIdx.z == 0 && p.bypass != nullptr && threadIdx.x < p.G && p.bypass[h0 + threadIdx.x])
+    sel_cnt[h0 + threadIdx.x] = 0;
 }
 
 int launch_build_step(const Params& p, const int* seq_lens, const int* page_table, void* k_pool, void* v_pool,
                       const void* k_new, const void* v_new, float* stats, void* summ, const int* sel_idx, int* sel_cnt,
-                      void* tiles, int* ntiles, float* out, float* lse, int* status, int* ticket,
-                      cudaStream_t stream) {
+                      void* tiles, int* ntiles, int* status, int* ticket, cudaStream_t stream) {
   const size_t smem = build_smem_bytes(p.mpp);
   // static + dynamic shared memory can pass the 48 KB default even when the
   // dynamic part alone does not: always opt in (cached per kernel)
   smem_limit_at_least(reinterpret_cast<const void*>(build_step_kernel), (int)smem);
-  const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B), dim3(kStepBuildThreads), smem, stream, p,
+  const cudaError_t e = launch_pdl(build_step_kernel, dim3(p.Hk, p.B, num_windows(p.mpp)), dim3(kStepBuildThreads),
+                                   smem, stream, p,
                                    seq_lens, page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
                                    static_cast<const __nv_bfloat16*>(v_new), stats, static_cast<__nv_bfloat16*>(summ),
-                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
+                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
@@ -111,8 +113,7 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
                     const int* __restrict__ page_table, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
                     const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new, float* stats,
                     __nv_bfloat16* __restrict__ summ, int* __restrict__ sel_idx, int* __restrict__ sel_cnt,
-                    Tile* __restrict__ tiles, int* __restrict__ ntiles, float* __restrict__ out,
-                    float* __restrict__ lse, int* status, int* ticket) {
+                    Tile* __restrict__ tiles, int* __restrict__ ntiles, int* status, int* ticket) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
@@ -159,8 +160,9 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
       summarize_block_warp(p, b, kvh, (L - 1) / p.bs[kvh], L, k_pool, page_table + (size_t)b * p.mpp, summ, status);
     return;
   }
-  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, s_sel, s_cnt, SA_SEL_BLOCK, tiles, ntiles, out,
-                                     lse, status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active);
+  build_unit_tiles<kStepTileThreads>(p, b, kvh, seq_lens, page_table, s_sel, s_cnt, SA_SEL_BLOCK, tiles, ntiles,
+                                     status, smem_b, reinterpret_cast<uint32_t*>(smem_b + win), scan_tmp, active, 0,
+                                     num_windows(p.mpp));
 }
 
 // SA_ERR_UNSUPPORTED when some head's candidates exceed the fused kernel's
@@ -168,14 +170,13 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
 // topk_kernel + build_step_kernel.
 int launch_select_build(const Params& p, const float* scores, const int* seq_lens, const int* page_table,
                         void* k_pool, void* v_pool, const void* k_new, const void* v_new, float* stats, void* summ,
-                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, float* out, float* lse, int* status,
-                        int* ticket, cudaStream_t stream) {
+                        int* sel_idx, int* sel_cnt, void* tiles, int* ntiles, int* status, int* ticket,
+                        cudaStream_t stream) {
   const int max_n = max_candidates(p);
   const size_t smem = build_smem_bytes(p.mpp) + ((size_t)p.G * p.kcap + p.G) * sizeof(int);
   if (smem > 160 * 1024) return SA_ERR_UNSUPPORTED;
   void (*kern)(Params, const float*, const int*, const int*, __nv_bfloat16*, __nv_bfloat16*, const __nv_bfloat16*,
-               const __nv_bfloat16*, float*, __nv_bfloat16*, int*, int*, Tile*, int*, float*, float*, int*,
-               int*) = nullptr;
+               const __nv_bfloat16*, float*, __nv_bfloat16*, int*, int*, Tile*, int*, int*, int*) = nullptr;
   const int v = (p.sel_mode == SA_SELECT_GROUP ? 2 : 0) | (k_new != nullptr ? 1 : 0);
 #define SA_SB_PICK(GG, KK)                                                             \
   (v == 0 ? select_build_kernel<GG, KK, false, false> : v == 1 ? select_build_kernel<GG, KK, false, true> \
@@ -193,7 +194,7 @@ int launch_select_build(const Params& p, const float* scores, const int* seq_len
                                    page_table, static_cast<__nv_bfloat16*>(k_pool),
                                    static_cast<__nv_bfloat16*>(v_pool), static_cast<const __nv_bfloat16*>(k_new),
                                    static_cast<const __nv_bfloat16*>(v_new), stats, static_cast<__nv_bfloat16*>(summ),
-                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, out, lse, status, ticket);
+                                   sel_idx, sel_cnt, static_cast<Tile*>(tiles), ntiles, status, ticket);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -47,9 +47,15 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
   return (size_t)w * (sizeof(int) + 4 * sizeof(uint32_t)) + 16;
 }
 
-// Collective over threads [0, NT) (named barrier 1): build the tile list of
-// unit (b, kvh).  Thread t owns the contiguous pages [t per, t per + per) of
-// each window.  Every global load is issued up front (sequence length, the
+// A unit's tile list is kept in segments, one per window of kWinPages pages:
+// the tiles of window w start at entry w * kWinPages of the unit's
+// max_pages_per_seq entries, and ntiles[unit * num_windows + w] counts them.
+// The windows of one unit can then be built by different CTAs.
+__host__ __device__ inline int num_windows(int mpp) { return (mpp + kWinPages - 1) / kWinPages; }
+
+// Collective over threads [0, NT) (named barrier 1): build the tile-list
+// segments of windows [w_first, w_first + w_count) of unit (b, kvh).  Thread
+// t owns the contiguous pages [t per, t per + per) of each window.  Every global load is issued up front (sequence length, the
 // first window's page-table entries, the thread's first selection entries),
 // then: dense-set masks, selected tokens OR-ed in (shared-memory atomics),
 // a block scan of the page flags, and one 32-byte store per tile.
@@ -57,15 +63,15 @@ __host__ __device__ inline size_t build_smem_bytes(int mpp) {
 // cnt_row: their counts [G].  A page's four mask words are one 16-byte
 // access (conflict-free across a warp's contiguous page ranges).  active: the heads that attend (G bits); the
 // others are left out -- no tokens attend for them and their output rows are
-// not written.  s_flag: window ints, s_mask: 4 window words,
+// not written.  A unit with no tile at all (L = 0) is answered by the
+// decode's merge (O = 0, lse = -inf).  s_flag: window ints, s_mask: 4 window words,
 // scan_tmp: 32 ints.
 template <int NT>
 __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh, const int* __restrict__ seq_lens,
                                                  const int* __restrict__ page_table, const int* sel_row,
                                                  const int* cnt_row, int gran, Tile* __restrict__ tiles,
-                                                 int* __restrict__ ntiles, float* __restrict__ out,
-                                                 float* __restrict__ lse, int* status, int* s_flag, uint32_t* s_mask,
-                                                 int* scan_tmp, uint32_t active) {
+                                                 int* __restrict__ ntiles, int* status, int* s_flag, uint32_t* s_mask,
+                                                 int* scan_tmp, uint32_t active, int w_first, int w_count) {
   constexpr int kPer = (kWinPages + NT - 1) / NT;   // pages per thread and window, at most
   constexpr int kItemRegs = 2;                      // selection entries prefetched per thread (r = 0, 1 below)
   auto bsync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); };
@@ -76,13 +82,15 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   const int* pt_row = page_table + (size_t)b * p.mpp;
   const int win = min(p.mpp, kWinPages);
   const int per = (win + NT - 1) / NT;
-  // ---- up-front loads
+  const int nwin = num_windows(p.mpp);
+  const int wp_first = w_first * kWinPages;   // first page of the first window
+  // ---- up-front loads (the first window's page-table entries)
   const int Lraw = seq_lens[b];
   int ptr[kPer];
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
     const int i = tid * per + r;
-    ptr[r] = (r < per && i < win) ? __ldg(pt_row + i) : -1;
+    ptr[r] = (r < per && i < win && wp_first + i < p.mpp) ? __ldg(pt_row + wp_first + i) : -1;
   }
   const int nitems = G * p.kcap;
   int icnt[kItemRegs], iidx[kItemRegs];
@@ -104,10 +112,14 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
   const int Bs = p.bs[kvh];
   const uint32_t all = active;
   Tile* T = tiles + (size_t)u * p.mpp;
-  int total = 0;
 
-  for (int w0 = 0; w0 < npg; w0 += kWinPages) {
-    const int wn = min(kWinPages, npg - w0);
+  for (int wi = w_first; wi < w_first + w_count; ++wi) {
+    const int w0 = wi * kWinPages;
+    const int wn = max(0, min(kWinPages, npg - w0));
+    if (wn == 0) {   // no page of the sequence in this window
+      if (tid == 0) ntiles[u * nwin + wi] = 0;
+      continue;
+    }
     const int a = min(wn, tid * per), e = min(wn, a + per);
     // dense-set tokens of each page attend for every head
     for (int i = a; i < e; ++i) {
@@ -174,13 +186,13 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
       if (lane < NT / 32) scan_tmp[lane] = y;
     }
     bsync();
-    int idx = total + (warp > 0 ? scan_tmp[warp - 1] : 0) + x - c;
+    int idx = w0 + (warp > 0 ? scan_tmp[warp - 1] : 0) + x - c;   // the window's segment starts at entry w0
     // one 32-byte descriptor per tile (the page-table entry prefetched when possible)
 #pragma unroll
     for (int r = 0; r < kPer; ++r) {
       const int i = a + r;
       if (r < per && i < e && s_flag[i]) {
-        const int ph = w0 == 0 ? ptr[r] : __ldg(pt_row + w0 + i);
+        const int ph = wi == w_first ? ptr[r] : __ldg(pt_row + w0 + i);
         const bool ok = ph >= 0 && ph < p.num_pages;
         if (!ok) set_status(status, SA_ERR_BAD_PAGE);
         int4* dst = reinterpret_cast<int4*>(T + idx);
@@ -190,14 +202,8 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
         ++idx;
       }
     }
-    total += scan_tmp[NT / 32 - 1];
+    if (tid == 0) ntiles[u * nwin + wi] = scan_tmp[NT / 32 - 1];
     bsync();   // the window's shared state is reused by the next window
-  }
-  if (tid == 0) ntiles[u] = total;
-  if (total == 0) {   // nothing attended (L = 0): O = 0, lse = -inf; the decode kernel skips the unit
-    for (int i = tid; i < G * kD; i += NT)
-      if ((active >> (i / kD)) & 1u) out[((size_t)b * p.Hq + kvh * G) * kD + i] = 0.f;
-    if (tid < G && ((active >> tid) & 1u)) lse[(size_t)b * p.Hq + kvh * G + tid] = -INFINITY;
   }
 }
 

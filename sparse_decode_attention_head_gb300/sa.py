@@ -88,6 +88,10 @@ def lib():
             "sa_head_sparsity": (ctypes.c_int, [P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp]),
             "sa_decode_step_bypass": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                                      vp, vp, vp, vp, vp, vp, vp, vp]),
+            "sa_step_plan_create": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                   ctypes.POINTER(vp)]),
+            "sa_step_plan_launch": (ctypes.c_int, [vp, vp]),
+            "sa_step_plan_destroy": (ctypes.c_int, [vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -432,3 +436,40 @@ class DecodeStepCall:
         rc = self._fn(*self._args, _stream())
         if rc != SA_OK:
             raise SAError(rc, "sa_decode_step")
+
+
+class StepPlan:
+    """sa_decode_step on fixed tensors, prepared once as a CUDA graph inside
+    the library (sa_step_plan_create); each call replays it on the current
+    stream with one graph launch (sa_step_plan_launch).  The tensors'
+    contents may change between calls; the object keeps them alive and frees
+    the plan when it is collected or closed."""
+
+    def __init__(self, prob: Problem, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out,
+                 lse, ws: Workspace):
+        _check_step_args(prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse)
+        self._keep = (prob, q, k_pool, v_pool, page_table, seq_lens, summaries, sel_idx, sel_cnt, out, lse, ws)
+        self._lib = lib()
+        h = ctypes.c_void_p()
+        _check(self._lib.sa_step_plan_create(prob.ref, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                             _ptr(seq_lens), _ptr(summaries), _ptr(sel_idx), _ptr(sel_cnt),
+                                             _ptr(out), _ptr(lse), _ptr(ws.buf), ctypes.byref(h)),
+               "sa_step_plan_create")
+        self._h = h
+        self._launch = self._lib.sa_step_plan_launch
+
+    def __call__(self):
+        rc = self._launch(self._h, _stream())
+        if rc != SA_OK:
+            raise SAError(rc, "sa_step_plan_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.sa_step_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -170,3 +170,18 @@ def test_misaligned_out_or_workspace_rejected_before_launch(lib):
     assert lib.sa_block_summarize(p.ref, a, a, a, 0, -1, a, m, None) == bad                         # ws
     assert lib.sa_score_blocks(p.ref, a, a, a, a, m, None) == bad                                   # ws
     assert lib.sa_select_topk(p.ref, a, a, a, a, a, None, m, None) == bad                           # ws
+
+
+def test_step_plan_refuses_bad_arguments_before_capture(lib):
+    # sa_step_plan_create checks like sa_decode_step and returns before capturing anything
+    p = _prob()
+    a, m = ctypes.c_void_p(256), ctypes.c_void_p(260)
+    h = ctypes.c_void_p()
+    bad = sa.SA_ERR_INVALID_ARG
+    assert lib.sa_step_plan_create(p.ref, a, a, a, a, a, a, a, a, m, a, a, ctypes.byref(h)) == bad   # out
+    assert lib.sa_step_plan_create(p.ref, None, a, a, a, a, a, a, a, a, a, a, ctypes.byref(h)) == bad  # q
+    assert lib.sa_step_plan_create(p.ref, a, a, a, a, a, a, a, a, a, a, a, None) == bad               # plan
+    assert h.value is None
+    assert lib.sa_step_plan_create(_prob(D=64).ref, a, a, a, a, a, a, a, a, a, a, a, ctypes.byref(h)) == bad
+    assert lib.sa_step_plan_launch(None, None) == bad
+    assert lib.sa_step_plan_destroy(None) == sa.SA_OK

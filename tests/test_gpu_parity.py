@@ -119,6 +119,16 @@ def test_full_budget_is_dense_attention():
             H.assert_close(out[b, h].cpu().numpy(), O, "dense O")
 
 
+def test_long_ragged_sequences_span_several_tile_windows():
+    # more than 4096 pages a sequence: each window of 4096 pages (65536
+    # tokens) gets its own tile-list segment and builder CTA.  The lengths end
+    # inside window 2, exactly on the window 0/1 edge, inside window 1 with
+    # window 2 empty, and at 0 (no tile at all: O = 0, lse = -inf).
+    wl = _small("long_ragged", B=4, L=150000, lens=[150000, 65536, 70001, 0], block_sizes=[16, 64],
+                budget_bp=[500, 500], W=1024, heavy_count=6, recency=2000)
+    _full_pipeline(wl, 7, "minmax")
+
+
 def test_zero_budget_is_dense_part_only():
     wl = _small(B=2)
     _full_pipeline(wl, 6, "mean", ks=[0] * wl.Hq)

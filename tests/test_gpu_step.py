@@ -115,6 +115,18 @@ def test_step_full_and_zero_budget_vs_oracle():
     _step_vs_oracle(wl, 35, "minmax", ks=ks)
 
 
+@pytest.mark.parametrize("block_sizes", [[16, 64], [64, 64]])
+def test_step_long_ragged_sequences_span_several_tile_windows(block_sizes):
+    # lengths past 4096 pages, ending inside window 2, on the window 0/1
+    # edge, inside window 1 and at 0.  Block size 16 gives more candidates
+    # than the fused top-k + build kernel holds (separate top-k, one builder
+    # CTA per window); block size 64 on both heads fits it (one CTA builds
+    # every window of its unit).
+    wl = _small("long_ragged", B=4, L=150000, lens=[150000, 65536, 70001, 0], block_sizes=block_sizes,
+                budget_bp=[500, 500], W=1024, heavy_count=6, recency=2000)
+    _step_vs_oracle(wl, 39, "minmax")
+
+
 def test_step_tiny_4k_new_inputs_each_call():
     # one workspace, fresh q and keys on every call: nothing of a previous step leaks into the next
     wl = synth.workload("tiny_4k")
@@ -134,3 +146,34 @@ def test_step_tiny_4k_new_inputs_each_call():
             assert np.array_equal(idx[b, h, :n].cpu().numpy(), sel)
             H.assert_close(out[b, h].cpu().numpy(), ref[(b, h)][0], "O")
             H.assert_close(lse[b, h:h + 1].cpu().numpy(), np.array([ref[(b, h)][1]]), "lse")
+
+
+def test_prepared_step_plan_matches_decode_step():
+    # sa_step_plan_* replays the step captured on fixed buffers; with fresh
+    # contents in those buffers it gives sa_decode_step's results, call after call
+    wl = synth.workload("tiny_4k")
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    ws = sa.Workspace(prob)
+    case = synth.make_decode_case(wl, 51)
+    dev = H.to_dev(case)
+    summ = H.gpu_summaries(prob, dev, ws)
+    idx = torch.empty(wl.B, wl.Hq, prob.kcap, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(wl.B, wl.Hq, dtype=torch.int32, device="cuda")
+    out = torch.empty(wl.B, wl.Hq, wl.D, device="cuda")
+    lse = torch.empty(wl.B, wl.Hq, device="cuda")
+    plan = sa.StepPlan(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx,
+                       cnt, out, lse, ws)
+    for seed in (52, 53, 54):
+        dev["q"].copy_(synth.make_decode_case(wl, seed).q.to("cuda"))
+        plan()
+        torch.cuda.synchronize()
+        o1, l1, i1, c1 = out.clone(), lse.clone(), idx.clone(), cnt.clone()
+        ri, rc, ro, rl = _run_step(prob, dev, summ, ws)
+        assert torch.equal(c1, rc)
+        for b in range(wl.B):
+            for h in range(wl.Hq):
+                assert torch.equal(i1[b, h, :int(rc[b, h])], ri[b, h, :int(rc[b, h])])
+        H.assert_close(o1.cpu().numpy(), ro.cpu().numpy(), "plan O")
+        H.assert_close(l1.cpu().numpy(), rl.cpu().numpy(), "plan lse")
+    plan.close()
