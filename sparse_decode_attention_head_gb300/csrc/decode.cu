@@ -251,6 +251,9 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   if (warp == kConsWarps) {
     const bool owner = lane < nslots;
     int use = 0;
+    // K / V pages are read once: they should not push the partials, tile
+    // lists and summaries out of L2
+    const uint64_t kv_policy = l2_evict_first();
     auto chunk_info = [&](int t) {
       ChunkInfo c;
       c.unit = -1;
@@ -350,8 +353,8 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               uint8_t* dst = s_tiles + (size_t)slot * kTileBytes;
               const int row = (phys * p.Hk + (ci.unit % p.Hk)) * kP;
               mbar_arrive_expect_tx(&s_full[slot], kTileBytes);
-              tma_load_3d(dst, &tmK, 0, row, 0, &s_full[slot]);
-              tma_load_3d(dst + kSlab, &tmV, 0, row, 0, &s_full[slot]);
+              tma_load_3d_hint(dst, &tmK, 0, row, 0, &s_full[slot], kv_policy);
+              tma_load_3d_hint(dst + kSlab, &tmV, 0, row, 0, &s_full[slot], kv_policy);
             } else {
               mbar_arrive(&s_full[slot]);
             }
@@ -658,7 +661,7 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 // chunks are issued together, then the running sums are rescaled once to
 // the batch's maximum and the batch is added.
 constexpr int kMergeThreads = kD;
-constexpr int kMergeIn = 16;
+constexpr int kMergeIn = 32;
 
 __global__ void __launch_bounds__(kMergeThreads)
 merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __restrict__ chunk_prefix,
