@@ -27,6 +27,16 @@ __device__ __forceinline__ void item_range(int gran, int x, int Bs, int Lc, int 
   }
 }
 
+// Bit r (r < 16) set when token t0 + r lies in [lo, hi).
+__device__ __forceinline__ uint32_t token_bits(int t0, int lo, int hi) {
+  const int a = min(max(lo - t0, 0), kP), b = min(max(hi - t0, 0), kP);
+  return b > a ? ((1u << b) - 1u) & ~((1u << a) - 1u) : 0u;
+}
+
+// Bit j of a 4-bit value moved to bit 8 j (the four products of the
+// multiplier land on distinct bits, so nothing carries).
+__device__ __forceinline__ uint32_t spread_nibble(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
 // G-bit mask of the unit's heads that attend: those not answered by the
 // sparsity bypass (all heads when p.bypass is NULL).
 __device__ __forceinline__ uint32_t unit_active_heads(const Params& p, int b, int kvh) {
@@ -121,20 +131,16 @@ __device__ __forceinline__ void build_unit_tiles(const Params& p, int b, int kvh
       continue;
     }
     const int a = min(wn, tid * per), e = min(wn, a + per);
-    // dense-set tokens of each page attend for every head
+    // dense-set tokens of each page attend for every head: the page's 16-bit
+    // token mask from the two dense ranges, each bit spread to a byte of `all`
     for (int i = a; i < e; ++i) {
+      const int t0 = (w0 + i) * kP;
+      const uint32_t tm = token_bits(t0, 0, s_end) | token_bits(t0, w_beg, Lc);
       uint32_t m[4];
 #pragma unroll
-      for (int w4 = 0; w4 < 4; ++w4) {
-        m[w4] = 0;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int tok = (w0 + i) * kP + 4 * w4 + r;
-          if (tok < Lc && (tok < s_end || tok >= w_beg)) m[w4] |= all << (8 * r);
-        }
-      }
+      for (int w4 = 0; w4 < 4; ++w4) m[w4] = spread_nibble((tm >> (4 * w4)) & 0xfu) * all;
       reinterpret_cast<uint4*>(s_mask)[i] = make_uint4(m[0], m[1], m[2], m[3]);
-      s_flag[i] = (m[0] | m[1] | m[2] | m[3]) != 0;
+      s_flag[i] = tm != 0u;
     }
     bsync();
     // each head's selected tokens inside M (and inside this window)

@@ -78,18 +78,33 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
   }
   uint32_t key[KPT];
   uint32_t kmin = 0xffffffffu, kmax = 0u;
+  // a thread's KPT consecutive scores as 16-byte loads when the row allows it
+  const bool vec = !ROWS && KPT % 4 == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0 && tg * KPT + KPT <= n;
+  if (vec) {
 #pragma unroll
-  for (int q = 0; q < KPT; ++q) {
-    const int i = tg * KPT + q;
-    float x = 0.f;
-    if (i < n) {
-      x = sc[i];
-      if (ROWS)
-        for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, sc[r * row_stride + i]);
+    for (int v = 0; v < KPT / 4; ++v) {
+      const float4 f = *reinterpret_cast<const float4*>(sc + tg * KPT + 4 * v);
+      key[4 * v] = order_key(f.x);
+      key[4 * v + 1] = order_key(f.y);
+      key[4 * v + 2] = order_key(f.z);
+      key[4 * v + 3] = order_key(f.w);
     }
-    key[q] = i < n ? order_key(x) : 0u;
-    if (i < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
+  } else {
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = tg * KPT + q;
+      float x = 0.f;
+      if (i < n) {
+        x = sc[i];
+        if (ROWS)
+          for (int r = 1; r < nrows; ++r) x = __fadd_rn(x, sc[r * row_stride + i]);
+      }
+      key[q] = i < n ? order_key(x) : 0u;
+    }
   }
+#pragma unroll
+  for (int q = 0; q < KPT; ++q)
+    if (tg * KPT + q < n) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
