@@ -353,8 +353,15 @@ int launch_topk(const Params& p, const float* scores, const int* seq_lens, int* 
   const int max_n = max_candidates(p);
   const bool grp = p.sel_mode == SA_SELECT_GROUP;
   cudaError_t e;
+  // the smallest CTA that holds every candidate, so that CTAs of many heads share an SM
   if (max_n <= 256 * 8)
     e = launch_pdl(grp ? topk_kernel<256, 8, true> : topk_kernel<256, 8, false>, grid, dim3(256), 0, stream, p,
+                   scores, seq_lens, sel_idx, sel_cnt);
+  else if (max_n <= 256 * 16)
+    e = launch_pdl(grp ? topk_kernel<256, 16, true> : topk_kernel<256, 16, false>, grid, dim3(256), 0, stream, p,
+                   scores, seq_lens, sel_idx, sel_cnt);
+  else if (max_n <= 512 * 16)
+    e = launch_pdl(grp ? topk_kernel<512, 16, true> : topk_kernel<512, 16, false>, grid, dim3(512), 0, stream, p,
                    scores, seq_lens, sel_idx, sel_cnt);
   else if (max_n <= 1024 * 16)
     e = launch_pdl(grp ? topk_kernel<1024, 16, true> : topk_kernel<1024, 16, false>, grid, dim3(1024), 0, stream, p,
