@@ -114,21 +114,23 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
                     const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new, float* stats,
                     __nv_bfloat16* __restrict__ summ, int* __restrict__ sel_idx, int* __restrict__ sel_cnt,
                     Tile* __restrict__ tiles, int* __restrict__ ntiles, int* status, int* ticket) {
+  // the call's sequence lengths are ready when this kernel starts (it is the
+  // second of the step): the candidate range is read before the wait
+  const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int L = min(seq_lens[b], p.mpp * kP);
+  int j0, j1;
+  candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0;   // the decode's chunk tickets
   extern __shared__ int smem_b[];   // window flags, window masks, then selections [G][kcap] and counts [G]
   __shared__ TopkScratch S[kStepBuildThreads / GROUP];
   __shared__ int scan_tmp[32];
-  const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int G = p.G;
   const int win = min(p.mpp, kWinPages);
   int* s_sel = smem_b + build_smem_bytes(p.mpp) / sizeof(int);
   int* s_cnt = s_sel + G * p.kcap;
-  const int L = min(seq_lens[b], p.mpp * kP);
   const uint32_t active = unit_active_heads(p, b, kvh);   // loaded now, used after the top-k
-  int j0, j1;
-  candidate_range(L, p.S, p.W, p.bs[kvh], j0, j1);
   const int g = tid / GROUP;
   if (GRP) {   // one list for the group, from the summed scores
     if (g == 0)
@@ -148,10 +150,13 @@ select_build_kernel(Params p, const float* __restrict__ scores, const int* __res
     if (tid < G && !((active >> tid) & 1u)) s_cnt[tid] = 0;
     __syncthreads();
   }
-  for (int i = tid; i < G * p.kcap; i += kStepBuildThreads)
-    if (i - (i / p.kcap) * p.kcap < s_cnt[i / p.kcap]) sel_idx[h0 * p.kcap + i] = s_sel[i];
-  if (tid < G) sel_cnt[h0 + tid] = s_cnt[tid];
   if (tid >= kStepTileThreads) {
+    // the selections out (the tile build reads them from shared memory and
+    // starts at once), then the append and the tail summary
+    const int lane = tid & 31;
+    for (int gg = 0; gg < G; ++gg)
+      for (int i = lane; i < s_cnt[gg]; i += 32) sel_idx[(h0 + gg) * p.kcap + i] = s_sel[gg * p.kcap + i];
+    if (lane < G) sel_cnt[h0 + lane] = s_cnt[lane];
     if (APPEND) {
       append_token_warp(p, b, kvh, L, k_new, v_new, k_pool, v_pool, page_table + (size_t)b * p.mpp, status);
       if (stats != nullptr) stats_add_new_warp(p, stats, k_new, v_new, b, kvh, L);   // read by the scores only

@@ -42,6 +42,7 @@ struct TopkScratch {
   uint32_t prefix;
   int krem;
   int bcnt;            // keys in the bucket holding the k-th key
+  int eqt;             // keys equal to the k-th key (from the small-bucket rank)
   int nc;              // keys gathered into cand
 };
 
@@ -119,6 +120,7 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
   uint32_t mask = common >= 32 ? 0xffffffffu : (common == 0 ? 0u : (0xffffffffu << (32 - common)));
   uint32_t prefix = gmin & mask;
   int krem = k;
+  int eq_total = common >= 32 ? n : -1;   // keys equal to the k-th key, once known
   for (int top = 32 - common; top > 0; top -= 8) {   // this pass resolves bits [shift, top)
     const int shift = max(0, top - 8);
     const uint32_t dmask = (1u << (top - shift)) - 1u;
@@ -153,6 +155,7 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
     group_sync(bar_id, GROUP);
     prefix = S.prefix;
     krem = S.krem;
+    eq_total = shift == 0 ? S.bcnt : -1;   // a pass that resolves the last bits leaves the equal keys
     mask |= dmask << shift;
     if (shift > 0 && S.bcnt <= 32) {
       // gather the bucket and let warp 0 rank its keys: the krem-th largest is T
@@ -174,11 +177,13 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
         if (lane < nc && gt_cnt < krem && krem <= ge_cnt) {   // every lane holding T agrees
           S.prefix = mine;
           S.krem = krem - gt_cnt;
+          S.eqt = ge_cnt - gt_cnt;
         }
       }
       group_sync(bar_id, GROUP);
       prefix = S.prefix;
       krem = S.krem;
+      eq_total = S.eqt;
       mask = 0xffffffffu;
       group_sync(bar_id, GROUP);
       break;
@@ -192,6 +197,16 @@ __device__ void group_topk(const float* __restrict__ sc, int n, int k_req, int b
   for (int q = 0; q < KPT; ++q) {
     const int i = tg * KPT + q;
     if (i < n) { eq += key[q] == T; gt += key[q] > T; }
+  }
+  if (eq_total == need_eq) {   // every key equal to T is taken (the usual case): one scan
+    int pos = group_excl_scan<GROUP>(gt + eq, S.red[1], bar_id);
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = tg * KPT + q;
+      if (i < n && key[q] >= T) out[pos++] = base_idx + i;
+    }
+    if (tg == 0) *cnt_out = k;
+    return;
   }
   const int eq_before = group_excl_scan<GROUP>(eq, S.red[0], bar_id);
   const int take = gt + max(0, min(eq, need_eq - eq_before));
