@@ -54,6 +54,31 @@ def test_noalloc_matches_workspace_decode_twice(name):
         assert int(status.item()) == sa.SA_OK
 
 
+def test_noalloc_vs_oracle_long_ragged_given_oracle_selections():
+    # the oracle's own index sets in, the fp64 oracle's O and lse out:
+    # lengths past 4096 pages (tile-list windows), ending inside window 2, on
+    # the window 0/1 edge, inside window 1, and at 0 (O = 0, lse = -inf)
+    wl = synth.Workload("long_ragged", B=4, Hq=6, Hk=2, L=150000, lens=[150000, 65536, 70001, 0],
+                        block_sizes=[16, 64], budget_bp=[500, 500], S=4, W=1024, c_heavy=2.0, heavy_count=6,
+                        recency=2000)
+    case = synth.make_decode_case(wl, 23)
+    nc = H.to_np_case(case)
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks)
+    ref_sel = H.oracle_select(nc, wl, ks, "minmax")
+    idx, cnt = H.sel_to_tensor(prob, {k: v[0] for k, v in ref_sel.items()})
+    dev = H.to_dev(case)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    o, l = _noalloc(prob, dev, idx, cnt, sa.SEL_BLOCK, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == sa.SA_OK
+    ref = H.oracle_decode(nc, wl, {k: v[0] for k, v in ref_sel.items()}, sa.SEL_BLOCK, prob.scale)
+    on, ln = o.cpu().numpy(), l.cpu().numpy()
+    for (b, h), (O, lz) in ref.items():
+        H.assert_close(on[b, h], O, f"noalloc O(b={b},h={h})")
+        H.assert_close(np.array([ln[b, h]]), np.array([lz]), f"noalloc lse(b={b},h={h})")
+
+
 def _tiny_setup(seed):
     wl = synth.workload("tiny_4k")
     case = synth.make_decode_case(wl, seed)
