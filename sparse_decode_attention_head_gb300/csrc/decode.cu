@@ -85,7 +85,6 @@ struct DecodeArgs {
   const Tile* tiles;
   const int* ntiles;
   float* partials;   // [chunks][partial_stride(G)]: per chunk O[G][kD], max[G], sum[G]
-  int* chunk_prefix; // [U + 1]: chunks before unit u (written by CTA 0 for the merge kernel)
   int nwin;          // tile-list segments (windows) per unit
   int* ticket;       // chunk ticket counter (zeroed by the tile builder)
   float* out;
@@ -236,8 +235,6 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
   __syncthreads();
   const int NCH = s_cprefix[SG];
   const int PS = partial_stride(G);
-  if (blockIdx.x == 0)   // chunks before unit u, for the merge kernel
-    for (int i = tid; i <= U; i += blockDim.x) A.chunk_prefix[i] = s_cprefix[i * NW];
 
   // ------------------------------------------------------------ producer warp
   // Takes chunks from the global ticket counter (one taken ahead) and
@@ -656,23 +653,48 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
 
 // One CTA per (query head g of the group, unit u): the exact log-sum-exp
 // merge of the unit's chunk partials in chunk order; thread d owns dim d.
-// Units held in one chunk (or none) were finished by the decode kernel.
+// Units held in one chunk were finished by the decode kernel.  The decode's
+// chunk list is a function of the tile counts and its grid, and the tile
+// builder had written the counts before the decode started (so before this
+// kernel was launched): the unit's first chunk and chunk count are derived
+// before the wait for the decode, and only the partials' loads follow it.
 // One pass with a running maximum: the (max, sum, O) loads of kMergeIn
 // chunks are issued together, then the running sums are rescaled once to
 // the batch's maximum and the batch is added.
 constexpr int kMergeThreads = kD;
-constexpr int kMergeIn = 32;
+constexpr int kMergeIn = 16;
 
 __global__ void __launch_bounds__(kMergeThreads)
-merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __restrict__ chunk_prefix,
-                    float* __restrict__ out, float* __restrict__ lse) {
+merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __restrict__ ntiles, int nwin,
+                    int decode_grid, float* __restrict__ out, float* __restrict__ lse) {
+  __shared__ int s_red[3][kMergeThreads / 32];
+  const int g = blockIdx.x, u = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int SG = p.B * p.Hk * nwin;
+  auto block_sum = [&](int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) t += red[w];
+    return t;
+  };
+  int tsum = 0;
+  for (int i = tid; i < SG; i += kMergeThreads) tsum += __ldg(ntiles + i);
+  const int T = block_sum(tsum, s_red[0]);   // the decode's chunk size, as it derives it
+  const int C = max(kMinChunk, (T + kChunksPerCta * decode_grid - 1) / (kChunksPerCta * decode_grid));
+  int before = 0, mine = 0;
+  for (int i = tid; i < (u + 1) * nwin; i += kMergeThreads) {
+    const int n = (__ldg(ntiles + i) + C - 1) / C;
+    if (i < u * nwin) before += n; else mine += n;
+  }
+  const int c0 = block_sum(before, s_red[1]), nch = block_sum(mine, s_red[2]);
   pdl_wait();
   pdl_trigger();
-  const int g = blockIdx.x, u = blockIdx.y;
-  const int c0 = chunk_prefix[u], nch = chunk_prefix[u + 1] - c0;
   if (nch == 1) return;   // written by the decode; no chunk (nothing attended): O = 0, lse = -inf below
   const int G = p.G, PS = partial_stride(G);
-  const int tid = threadIdx.x;
   const float* P = partials + (size_t)c0 * PS;
   float M = -INFINITY, acc = 0.f, l = 0.f;
   for (int j0 = 0; j0 < nch; j0 += kMergeIn) {
@@ -762,7 +784,7 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
 }
 
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
-                  float* partials, int* counters, float* out, float* lse, float* logits, int* status,
+                  float* partials, int* ticket, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
   const int U = p.B * p.Hk;
   const int SG = U * num_windows(p.mpp);
@@ -780,9 +802,8 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   A.tiles = static_cast<const Tile*>(tiles);
   A.ntiles = ntiles;
   A.partials = partials;
-  A.chunk_prefix = counters;
   A.nwin = num_windows(p.mpp);
-  A.ticket = counters + U + 1;
+  A.ticket = ticket;
   A.out = out;
   A.lse = lse;
   A.logits = logits;
@@ -790,7 +811,7 @@ int launch_decode(const Params& p, const void* q, const int* page_table, const v
   cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, stream, p, A, tmK, tmV, nslots);
   if (e != cudaSuccess) return SA_ERR_CUDA;
   e = launch_pdl(merge_chunks_kernel, dim3(p.G, U), dim3(kMergeThreads), 0, stream, p,
-                 static_cast<const float*>(partials), static_cast<const int*>(counters), out, lse);
+                 static_cast<const float*>(partials), ntiles, A.nwin, grid, out, lse);
   return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -22,7 +22,7 @@ int launch_build_tiles(const Params& p, const int* seq_lens, const int* page_tab
                        const int* sel_cnt, int gran, void* tiles, int* ntiles, int* status, int* ticket,
                        cudaStream_t stream);
 int launch_decode(const Params& p, const void* q, const int* page_table, const void* tiles, const int* ntiles,
-                  float* partials, int* counters, float* out, float* lse, float* logits, int* status,
+                  float* partials, int* ticket, float* out, float* lse, float* logits, int* status,
                   const CUtensorMap& tmK, const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
 size_t decode_smem_bytes(const Params& p);
 size_t decode_partials_bytes(const Params& p);

@@ -2,7 +2,7 @@
 // allocate device memory.
 //
 // sa_sparse_decode needs a caller-allocated workspace for its scratch (the
-// per-KV-head tile lists, the split-K chunk partials, the chunk prefix and
+// per-KV-head tile lists and their counts, the split-K chunk partials and
 // the chunk ticket).
 // Some callers cannot provide one: code that runs inside a host framework
 // which owns every device allocation through its own pool and forbids any
@@ -75,7 +75,7 @@ unsigned long long current_context_id() {
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct NoAllocLayout {
-  size_t status, counters, ntiles, tiles, partials, total;
+  size_t status, ticket, ntiles, tiles, partials, total;
 };
 
 NoAllocLayout layout_of(const sa::Params& p) {
@@ -83,8 +83,8 @@ NoAllocLayout layout_of(const sa::Params& p) {
   size_t off = 0;
   l.status = off;
   off = up256(off + sizeof(int));
-  l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
-  off = up256(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
+  l.ticket = off;   // the decode's chunk ticket (zeroed by the tile builder)
+  off = up256(off + sizeof(int));
   l.ntiles = off;   // tile counts per (unit, window)
   off = up256(off + sa::ntiles_bytes(p));
   l.tiles = off;
@@ -146,14 +146,14 @@ extern "C" int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* b = static_cast<char*>(base);
   int* status = status_or_null ? status_or_null : reinterpret_cast<int*>(b + l.status);
-  int* counters = reinterpret_cast<int*>(b + l.counters);
+  int* ticket = reinterpret_cast<int*>(b + l.ticket);
   // what must start at zero: the status word (the tile builder zeroes the
-  // chunk ticket; the decode writes the chunk prefix before the merge reads it)
+  // chunk ticket)
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return SA_ERR_CUDA;
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, b + l.tiles,
-                              reinterpret_cast<int*>(b + l.ntiles), status, counters + p.B * p.Hk + 1, s);
+                              reinterpret_cast<int*>(b + l.ntiles), status, ticket, s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, b + l.tiles, reinterpret_cast<int*>(b + l.ntiles),
-                           reinterpret_cast<float*>(b + l.partials), counters, out, lse, logits_or_null, status,
+                           reinterpret_cast<float*>(b + l.partials), ticket, out, lse, logits_or_null, status,
                            tmK, tmV, nsm, s);
 }

@@ -72,7 +72,7 @@ int make_params(const sa_problem* pr, Params* p) {
 }
 
 struct Layout {
-  size_t header, scores, tiles, ntiles, counters, partials, stage, total;
+  size_t header, scores, tiles, ntiles, ticket, partials, stage, total;
 };
 
 Layout layout_of(const Params& p) {
@@ -86,8 +86,8 @@ Layout layout_of(const Params& p) {
   off = align_up(off + sa::tiles_bytes(p));
   l.ntiles = off;   // tile counts per (unit, window)
   off = align_up(off + sa::ntiles_bytes(p));
-  l.counters = off;   // U + 1 chunk prefix entries, then the decode's chunk ticket
-  off = align_up(off + ((size_t)p.B * p.Hk + 2) * sizeof(int));
+  l.ticket = off;   // the decode's chunk ticket (zeroed by the tile builder)
+  off = align_up(off + sizeof(int));
   l.partials = off;
   off = align_up(off + sa::decode_partials_bytes(p));
   l.stage = off;   // score-table candidates per chunk
@@ -293,10 +293,10 @@ int sa_sparse_decode(const sa_problem* prob, const void* q, const void* k_pool, 
   cudaStream_t s = as_stream(stream);
   rc = sa::launch_build_tiles(p, seq_lens, page_table, sel_idx, sel_cnt, sel_granularity, at<void>(ws, l.tiles),
                               at<int>(ws, l.ntiles), at<int>(ws, l.header),
-                              at<int>(ws, l.counters) + p.B * p.Hk + 1, s);
+                              at<int>(ws, l.ticket), s);
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles),
-                           at<float>(ws, l.partials), at<int>(ws, l.counters), out, lse, logits_or_null,
+                           at<float>(ws, l.partials), at<int>(ws, l.ticket), out, lse, logits_or_null,
                            at<int>(ws, l.header), tmK, tmV, nsm, s);
 }
 
@@ -350,7 +350,7 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   if ((rc = sa::launch_score(p, q, summaries, seq_lens, scores, 0, nsm, s, kv_stats ? &E : nullptr)) != SA_OK)
     return rc;
   if (kv_stats != nullptr) p.bypass = bypass;
-  int* ticket = at<int>(ws, l.counters) + p.B * p.Hk + 1;
+  int* ticket = at<int>(ws, l.ticket);
   rc = sa::launch_select_build(p, scores, seq_lens, page_table, kp, vp, k_new, v_new, kv_stats, summaries, sel_idx,
                                sel_cnt, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), status, ticket, s);
   if (rc == SA_ERR_UNSUPPORTED) {   // candidates beyond the fused kernel's capacity: two kernels
@@ -360,7 +360,7 @@ int decode_step_impl(const sa_problem* prob, const void* q, const void* k_new, c
   }
   if (rc != SA_OK) return rc;
   return sa::launch_decode(p, q, page_table, at<void>(ws, l.tiles), at<int>(ws, l.ntiles), at<float>(ws, l.partials),
-                           at<int>(ws, l.counters), out, lse, nullptr, status, tmK, tmV, nsm, s);
+                           ticket, out, lse, nullptr, status, tmK, tmV, nsm, s);
 }
 
 }  // namespace sa_host
