@@ -115,8 +115,8 @@ def test_step_full_and_zero_budget_vs_oracle():
     _step_vs_oracle(wl, 35, "minmax", ks=ks)
 
 
-@pytest.mark.parametrize("block_sizes", [[16, 64], [64, 64]])
-def test_step_long_ragged_sequences_span_several_tile_windows(block_sizes):
+@pytest.mark.parametrize("block_sizes,mode", [([16, 64], "minmax"), ([64, 64], "minmax"), ([16, 64], "mean")])
+def test_step_long_ragged_sequences_span_several_tile_windows(block_sizes, mode):
     # lengths past 4096 pages, ending inside window 2, on the window 0/1
     # edge, inside window 1 and at 0.  Block size 16 gives more candidates
     # than the fused top-k + build kernel holds (separate top-k, one builder
@@ -124,7 +124,7 @@ def test_step_long_ragged_sequences_span_several_tile_windows(block_sizes):
     # every window of its unit).
     wl = _small("long_ragged", B=4, L=150000, lens=[150000, 65536, 70001, 0], block_sizes=block_sizes,
                 budget_bp=[500, 500], W=1024, heavy_count=6, recency=2000)
-    _step_vs_oracle(wl, 39, "minmax")
+    _step_vs_oracle(wl, 39, mode)
 
 
 def test_step_tiny_4k_new_inputs_each_call():
