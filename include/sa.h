@@ -334,8 +334,9 @@ int sa_update_score_tables(const sa_problem* prob, const float* vert_in,
  * (cudaGetSymbolAddress) with that device current, and again after the
  * device's context changes (cudaDeviceReset); make that first call before
  * any stream capture.  All calls share the array and it keeps the last
- * call's contents (the counters and status it needs zeroed are cleared at the
- * start of each call): calls that overlap on the GPU race with each other. */
+ * call's contents (the status word is cleared at the start of each call and
+ * the chunk ticket by the call's first kernel): calls that overlap on the
+ * GPU race with each other. */
 int sa_sparse_decode_noalloc(const sa_problem* prob, const void* q,
                              const void* k_pool, const void* v_pool,
                              const int32_t* page_table, const int32_t* seq_lens,

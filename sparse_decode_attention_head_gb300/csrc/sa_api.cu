@@ -396,7 +396,9 @@ int sa_step_plan_create(const sa_problem* prob, const void* q, const void* k_poo
     return SA_ERR_INVALID_ARG;
   cudaStream_t cs = nullptr;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return SA_ERR_CUDA;
-  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+  // relaxed: a first call in the process sets kernel attributes and queries
+  // occupancy while capturing
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
     cudaStreamDestroy(cs);
     return SA_ERR_CUDA;
   }

@@ -177,3 +177,41 @@ def test_prepared_step_plan_matches_decode_step():
         H.assert_close(o1.cpu().numpy(), ro.cpu().numpy(), "plan O")
         H.assert_close(l1.cpu().numpy(), rl.cpu().numpy(), "plan lse")
     plan.close()
+
+
+_FIRST_CALL = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+from sparse_decode_attention_head_gb300 import sa, synth
+from tests import harness as H
+wl = synth.workload("tiny_4k")
+ks = synth.k_per_qhead(wl)
+prob = H.make_problem(wl, ks)
+ws = sa.Workspace(prob)
+dev = H.to_dev(synth.make_decode_case(wl, 55))
+summ = torch.zeros(prob.summary_shape(), dtype=torch.bfloat16, device="cuda")
+bufs = [torch.empty(wl.B, wl.Hq, prob.kcap, dtype=torch.int32, device="cuda"),
+        torch.empty(wl.B, wl.Hq, dtype=torch.int32, device="cuda"),
+        torch.empty(wl.B, wl.Hq, wl.D, device="cuda"), torch.empty(wl.B, wl.Hq, device="cuda")]
+# the plan is the process's first step call: kernel attributes are set while capturing
+plan = sa.StepPlan(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, *bufs, ws)
+sa.block_summarize(prob, dev["k_pool"], dev["page_table"], dev["seq_lens"], summ, ws)
+plan()
+torch.cuda.synchronize()
+o1 = bufs[2].clone()
+sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, *bufs, ws)
+torch.cuda.synchronize()
+assert ws.status() == sa.SA_OK
+assert torch.allclose(o1, bufs[2], atol=1e-6, rtol=0), "plan and step differ"
+plan.close()
+print("ok")
+"""
+
+
+def test_step_plan_as_the_first_call_of_a_process():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
