@@ -72,3 +72,36 @@ def test_group_decode_step_matches_oracle():
     for (b, h), (O, l) in ref.items():
         H.assert_close(o_np[b, h], O, f"group decode O (b={b}, h={h})")
         H.assert_close(np.array([l_np[b, h]]), np.array([l]), f"group decode lse (b={b}, h={h})")
+
+
+def test_group_step_long_ragged_sequences_span_several_tile_windows():
+    # more candidates than the fused select/build kernel holds: the group top-k
+    # kernel, then one tile-builder CTA per 4096-page window; lengths end
+    # inside window 2, on the window 0/1 edge, inside window 1 and at 0
+    wl = synth.Workload("long_ragged", B=4, Hq=6, Hk=2, L=150000, lens=[150000, 65536, 70001, 0],
+                        block_sizes=[16, 64], budget_bp=[500, 500], S=4, W=1024, c_heavy=2.0, heavy_count=6,
+                        recency=2000)
+    case = synth.make_decode_case(wl, 12)
+    nc = H.to_np_case(case)
+    ks = synth.k_per_qhead(wl)
+    prob = H.make_problem(wl, ks, selection=sa.SELECT_GROUP)
+    dev = H.to_dev(case)
+    ws = sa.Workspace(prob)
+    summ = H.gpu_summaries(prob, dev, ws)
+    idx = torch.full((wl.B, wl.Hq, prob.kcap), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((wl.B, wl.Hq), -5, dtype=torch.int32, device="cuda")
+    out = torch.empty(wl.B, wl.Hq, wl.D, device="cuda")
+    lse = torch.empty(wl.B, wl.Hq, device="cuda")
+    sa.decode_step(prob, dev["q"], dev["k_pool"], dev["v_pool"], dev["page_table"], dev["seq_lens"], summ, idx, cnt,
+                   out, lse, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == sa.SA_OK
+    ref = H.oracle_select_group(nc, wl, ks, "minmax")
+    idx_np, cnt_np = idx.cpu().numpy(), cnt.cpu().numpy()
+    for (b, h), (sel, _, _) in ref.items():
+        assert np.array_equal(idx_np[b, h, :cnt_np[b, h]], sel), f"(b={b}, h={h}) group selection differs"
+    dec = H.oracle_decode(nc, wl, {k: v[0] for k, v in ref.items()}, sa.SEL_BLOCK, prob.scale)
+    o_np, l_np = out.cpu().numpy(), lse.cpu().numpy()
+    for (b, h), (O, lz) in dec.items():
+        H.assert_close(o_np[b, h], O, f"O(b={b},h={h})")
+        H.assert_close(np.array([l_np[b, h]]), np.array([lz]), f"lse(b={b},h={h})")

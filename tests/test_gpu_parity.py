@@ -129,6 +129,37 @@ def test_long_ragged_sequences_span_several_tile_windows():
     _full_pipeline(wl, 7, "minmax")
 
 
+def test_token_selections_on_long_ragged_sequences():
+    # token granularity through sa_sparse_decode across tile-list windows:
+    # per head a seeded set of tokens of the middle region (some repeated,
+    # some outside it, which must be ignored)
+    wl = _small("long_ragged", B=3, L=150000, lens=[150000, 70001, 0], block_sizes=[16, 64],
+                budget_bp=[500, 500], W=1024, heavy_count=6, recency=2000)
+    case = synth.make_decode_case(wl, 8)
+    nc = H.to_np_case(case)
+    ks = synth.k_per_qhead(wl)
+    kcap = 1200
+    prob = H.make_problem(wl, ks, kcap=kcap)
+    rng = np.random.default_rng(8)
+    sel, ref_sel = {}, {}
+    for b in range(wl.B):
+        L = int(nc.seq_lens[b])
+        for h in range(wl.Hq):
+            s_end, w_beg = min(L, wl.S), max(L - wl.W, min(L, wl.S))
+            toks = np.sort(rng.choice(np.arange(s_end, w_beg), size=min(1000, max(0, w_beg - s_end)), replace=False)) \
+                if w_beg > s_end else np.zeros(0, np.int64)
+            ref_sel[(b, h)] = toks
+            extra = list(toks[:50]) + [L + 5, -1]   # repeats and entries outside the middle region
+            sel[(b, h)] = np.array(list(toks) + extra, dtype=np.int64)
+    idx, cnt = H.sel_to_tensor(prob, sel)
+    dev = H.to_dev(case)
+    ws = sa.Workspace(prob)
+    out, lse = H.gpu_decode(prob, dev, idx, cnt, ws, gran=sa.SEL_TOKEN)
+    ref = H.oracle_decode(nc, wl, ref_sel, sa.SEL_TOKEN, prob.scale)
+    _check_decode(out, lse, ref)
+    assert ws.status() == sa.SA_OK
+
+
 def test_zero_budget_is_dense_part_only():
     wl = _small(B=2)
     _full_pipeline(wl, 6, "mean", ks=[0] * wl.Hq)
