@@ -144,8 +144,6 @@ template <bool LOGITS>
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, int nslots) {
-  pdl_wait();
-  pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int G = p.G;
@@ -181,12 +179,18 @@ decode_kernel(Params p, DecodeArgs A, const __grid_constant__ CUtensorMap tmK,
     s_misc[19] = 0;
     s_misc[20] = 0;
   }
-  if (p.bypass != nullptr)   // heads answered by the sparsity bypass: their rows are not written
+  // heads answered by the sparsity bypass: their rows are not written.  The
+  // flags are complete before this kernel starts (a call input, or written
+  // by the step's score kernel, which the tile builder waited for), so they
+  // are read before the wait for the tile builder.
+  if (p.bypass != nullptr)
     for (int i = tid; i < U; i += blockDim.x) {
       int m = 0;
       for (int g = 0; g < G; ++g) m |= (p.bypass[(size_t)i * G + g] != 0 ? 1 : 0) << g;
       s_umask[i] = (uint8_t)m;
     }
+  pdl_wait();
+  pdl_trigger();
   // prefix over the segments' tile counts (block-wide scan); the chunk size
   // follows from the total so that every CTA derives the same chunk list
   const int per = (SG + blockDim.x - 1) / blockDim.x;
@@ -691,6 +695,8 @@ merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __r
     if (i < u * nwin) before += n; else mine += n;
   }
   const int c0 = block_sum(before, s_red[1]), nch = block_sum(mine, s_red[2]);
+  const size_t row = (size_t)(u / p.Hk) * p.Hq + (u % p.Hk) * p.G + g;
+  const bool left_out = p.bypass != nullptr && p.bypass[row];   // complete before the decode started
   pdl_wait();
   pdl_trigger();
   if (nch == 1) return;   // written by the decode; no chunk (nothing attended): O = 0, lse = -inf below
@@ -727,9 +733,7 @@ merge_chunks_kernel(Params p, const float* __restrict__ partials, const int* __r
     }
     M = Mb;
   }
-  const int b = u / p.Hk, kvh = u % p.Hk;
-  const size_t row = (size_t)b * p.Hq + kvh * G + g;
-  if (p.bypass != nullptr && p.bypass[row]) return;
+  if (left_out) return;
   out[row * kD + tid] = l > 0.f ? acc / l : 0.f;
   if (tid == 0) lse[row] = l > 0.f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
 }
