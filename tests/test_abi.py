@@ -185,3 +185,22 @@ def test_step_plan_refuses_bad_arguments_before_capture(lib):
     assert lib.sa_step_plan_create(_prob(D=64).ref, a, a, a, a, a, a, a, a, a, a, a, ctypes.byref(h)) == bad
     assert lib.sa_step_plan_launch(None, None) == bad
     assert lib.sa_step_plan_destroy(None) == sa.SA_OK
+
+
+def test_workspace_grows_with_tile_list_windows():
+    # tile lists are kept in segments of 4096 pages, with a count and room
+    # for a chunk partial per (unit, window): crossing into a new window adds
+    # that room, a page inside a window does not
+    from sparse_decode_attention_head_gb300 import sa
+
+    def size(mpp):
+        p = sa.Problem(B=2, Hq=8, Hk=2, max_pages_per_seq=mpp, num_pages=2 * mpp, sink=4, window=64,
+                       block_sizes=[16, 16], k_per_head=[8] * 8, kcap=8)
+        n = sa.lib().sa_workspace_size(p.ref)
+        assert n > 0
+        return n
+
+    inside = size(8192) - size(8191)   # windows 2 -> 2
+    across = size(8193) - size(8192)   # windows 2 -> 3
+    # 4 units x one partial of G (128 + 2) fp32 = 2080 bytes each, less alignment slack
+    assert across - inside > 4 * 2080 - 2048
